@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunked Gated DeltaNet prefill (one JSON line on stdout).
+
+Default workload: B=1, T=4096, Hk=16, Hv=32, dk=dv=128 (bf16 q/k/v, fp32 g/beta,
+zero initial state, fp32 final state), synthetic and seeded.  A "step" is one
+gdn_prefill call over that batch (all kernels of the path).  The inputs (~104 MB)
+fit in L2, so a 256 MB buffer is written between timed steps to flush it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the path has
+no exchange step) and rank 0 prints the whole-job line.  ``--impl reference``
+times the float64 CPU oracle on the host cores instead (its only other user).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from hybrid_linear_attention_prefill_gb300.inputs import HEADLINE, WORKLOADS, workload  # noqa: E402
+
+METRIC = "Gated DeltaNet prefill tokens/s at T=4096,Hv=32; % of GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+CHUNK = 64
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes and flops (per workload)
+# ---------------------------------------------------------------------------
+def algorithmic(inp):
+    """Bytes each tensor of the path must move once, and the triangular-half flops."""
+    Tt, Hk, Hv, dk, dv, B = inp.total_tokens, inp.Hk, inp.Hv, inp.dk, inp.dv, inp.B
+    qk = 2 * Tt * Hk * dk * 2
+    vv = Tt * Hv * dv * 2
+    oo = Tt * Hv * dv * 2
+    gb = 2 * Tt * Hv * 4
+    st = B * Hv * dv * dk * 4
+    init = st if inp.init is not None else 0
+    cu = 4 * (B + 1) if inp.cu_seqlens is not None else 0
+    total = qk + vv + oo + gb + st + init + cu
+    flops = Tt * Hv * (CHUNK * (3 * dk + 2 * dv) + 6 * dk * dv)
+    # per kernel: preparation reads q, k, g, beta; the state carry reads q, k, v, g,
+    # beta (and the initial state) and writes o and the final state
+    return dict(total=total, flops=flops, prep=qk + gb + cu, chain=total)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, source="fallback")
+
+    def find(keys):
+        for k in keys:
+            if k in d and isinstance(d[k], (int, float)):
+                return float(d[k])
+        for v in d.values():
+            if isinstance(v, dict):
+                for k in keys:
+                    if k in v and isinstance(v[k], (int, float)):
+                        return float(v[k])
+        return None
+
+    hbm = find(["hbm_gbs", "hbm_GBps", "hbm_gb_s"])
+    bf16 = find(["bf16_tflops", "bf16_TFLOPs"])
+    return dict(hbm=hbm or FALLBACK_HBM_GBS, bf16=bf16 or FALLBACK_BF16_TFLOPS,
+                source="measured" if hbm else "fallback")
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "hybrid_linear_attention_prefill_gb300", "csrc", rec["source"])
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if sha != rec.get("source_sha256_16"):
+        return None
+    return rec
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def to_device(inp, torch, dev):
+    def t(a, dt=None):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        return (x.view(dt) if dt is not None else x).to(dev)
+
+    return dict(q=t(inp.q.view(np.int16), torch.bfloat16), k=t(inp.k.view(np.int16), torch.bfloat16),
+                v=t(inp.v.view(np.int16), torch.bfloat16), g=t(inp.g), beta=t(inp.beta),
+                cu=None if inp.cu_seqlens is None else t(inp.cu_seqlens),
+                init=None if inp.init is None else t(inp.init))
+
+
+def cpu_baseline_oracle(inp, target_s=8.0):
+    """Time the float64 oracle as it stands on the host cores on a bounded sample:
+    all value heads of the first `n` tokens of every sequence, n sized to ~target_s."""
+    import oracle
+
+    cores = oracle.num_cpus()
+    # calibrate on a small slice
+    n_cal = min(256, inp.total_tokens)
+    sub = slice_tokens(inp, n_cal)
+    t0 = time.perf_counter()
+    oracle.prefill_inputs(sub, want_final=False, nthreads=cores)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(min(inp.total_tokens, max(n_cal, n_cal * target_s / dt)))
+    sub = slice_tokens(inp, n)
+    t0 = time.perf_counter()
+    oracle.prefill_inputs(sub, want_final=True, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": sub.total_tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {sub.total_tokens} of {inp.total_tokens} tokens, all {inp.Hv} value heads, "
+                      f"float64 token loop, {dt:.2f} s wall"}
+
+
+def slice_tokens(inp, n):
+    """The first n tokens of a single-sequence problem (packed problems: the first sequences)."""
+    import copy
+
+    s = copy.copy(inp)
+    if inp.cu_seqlens is None and inp.B == 1:
+        for f in ("q", "k", "v", "g", "beta"):
+            setattr(s, f, getattr(inp, f)[:n])
+        s.T = n
+        return s
+    # packed or batched: keep whole sequences until n tokens are covered
+    bounds = inp.seq_bounds()
+    keep = 0
+    for i, (a, b) in enumerate(bounds):
+        keep = i + 1
+        if b >= n:
+            break
+    end = bounds[keep - 1][1]
+    for f in ("q", "k", "v", "g", "beta"):
+        setattr(s, f, getattr(inp, f)[:end])
+    s.B = keep
+    if inp.cu_seqlens is not None:
+        s.cu_seqlens = inp.cu_seqlens[:keep + 1].copy()
+        s.T = end
+    if inp.init is not None:
+        s.init = inp.init[:keep]
+    return s
+
+
+def run_gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from hybrid_linear_attention_prefill_gb300 import build as gbuild
+    from hybrid_linear_attention_prefill_gb300 import gdn
+
+    if rank == 0:
+        gbuild.build()
+    if world > 1:
+        dist.barrier()
+    gdn.load()
+
+    inp = workload(args.workload, seed=args.seed + rank)  # independent candidates per replica
+    d = to_device(inp, torch, dev)
+    Tt, B = inp.total_tokens, inp.B
+    out = torch.empty((Tt, inp.Hv, inp.dv), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((B, inp.Hv, inp.dv, inp.dk), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        return gdn.gdn_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], d["init"], out, fin,
+                               B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        gdn.check(step())
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for e3 in ev:  # create the handles before the timed region
+        for e in e3:
+            e.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.1)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        gdn.gdn_set_phase_events(ev[i][0], ev[i][1], ev[i][2])
+        gdn.check(step())
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    prep_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    chain_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    ms = statistics.mean(step_ms)
+    t_max = ms
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+
+    peaks = read_peaks()
+    alg = algorithmic(inp)
+    kernels = {"gdn_prep_kernel": statistics.mean(prep_ms), "gdn_chain_kernel": statistics.mean(chain_ms)}
+    dom = max(kernels, key=kernels.get)
+    dom_bytes = alg["chain"] if dom == "gdn_chain_kernel" else alg["prep"]
+    achieved = dom_bytes / (kernels[dom] * 1e-3) / 1e9
+    trec = traffic_record(dom)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
+                "traffic": None if trec is None else trec["dram_bytes_per_launch"],
+                "peak_source": peaks["source"]}
+    t_hbm = alg["total"] / (peaks["hbm"] * 1e9)
+    t_tc = alg["flops"] / (peaks["bf16"] * 1e12)
+    path_roof = {"roofline_us": round(max(t_hbm, t_tc) * 1e6, 2), "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                 "frac": round(max(t_hbm, t_tc) / (t_max * 1e-3), 4),
+                 "tflops": round(alg["flops"] / (t_max * 1e-3) / 1e12, 2),
+                 "algorithmic_bytes": alg["total"], "algorithmic_flops": alg["flops"]}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(inp, gdn, torch, stream, max(3, min(args.e2e_steps, K)))
+        if world > 1:
+            tt = torch.tensor([e2e.pop("_ms")], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e["value"] = world * Tt / (float(tt.item()) * 1e-3)
+        else:
+            e2e["value"] = Tt / (e2e.pop("_ms") * 1e-3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_oracle(inp)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": world * Tt / (t_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv,
+                       "dk": inp.dk, "dv": inp.dv, "tokens": Tt,
+                       "l2": "flushed between timed steps (256 MB write)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "path_roofline": path_roof,
+            "kernels_us": {k: round(v * 1e3, 2) for k, v in kernels.items()},
+            "ms_per_step_min": min(step_ms), "wall_s": round(wall, 3),
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": K * (2 + (inp.cu_seqlens is not None)),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def measure_e2e(inp, gdn, torch, stream, steps):
+    """The public host-buffer entry point, copies inside the timed region."""
+
+    def pinned(a):
+        t = torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        return t
+
+    q, k, v = pinned(inp.q.view(np.int16)), pinned(inp.k.view(np.int16)), pinned(inp.v.view(np.int16))
+    g, beta = pinned(inp.g), pinned(inp.beta)
+    cu = None if inp.cu_seqlens is None else pinned(inp.cu_seqlens)
+    init = None if inp.init is None else pinned(inp.init)
+    out = torch.empty((inp.total_tokens, inp.Hv, inp.dv), dtype=torch.int16).pin_memory()
+    fin = torch.empty((inp.B, inp.Hv, inp.dv, inp.dk), dtype=torch.float32).pin_memory()
+    args = (q, k, v, g, beta, cu, init, out, fin, inp.B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, stream)
+    for _ in range(2):
+        gdn.check(gdn.gdn_prefill_host(*args))
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        gdn.check(gdn.gdn_prefill_host(*args))
+        times.append(time.perf_counter() - t0)
+    h2d = sum(x.numel() * x.element_size() for x in (q, k, v, g, beta, cu, init) if x is not None)
+    d2h = out.numel() * 2 + fin.numel() * 4
+    return {"_ms": statistics.mean(times) * 1e3, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "api": "gdn_prefill_host (pinned host buffers)"}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the float64 oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    inp = workload(args.workload, seed=args.seed)
+    cores = oracle.num_cpus()
+    # size each step so that warmup + steps take about a minute in total
+    n_cal = min(128, inp.total_tokens)
+    t0 = time.perf_counter()
+    oracle.prefill_inputs(slice_tokens(inp, n_cal), want_final=False, nthreads=cores)
+    per_tok = max(time.perf_counter() - t0, 1e-5) / n_cal
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    n = int(max(16, min(inp.total_tokens, budget / per_tok)))
+    sub = slice_tokens(inp, n)
+    for _ in range(args.warmup):
+        oracle.prefill_inputs(sub, nthreads=cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.prefill_inputs(sub, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = sub.total_tokens / (ms * 1e-3)
+    sample = (f"first {sub.total_tokens} of {inp.total_tokens} tokens, all {inp.Hv} value heads per step, "
+              "float64 token loop")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": inp.B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv,
+                   "dk": inp.dk, "dv": inp.dv, "tokens": inp.total_tokens},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference_arm(args)
+    else:
+        run_gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

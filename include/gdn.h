@@ -1,0 +1,123 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) chunked Gated DeltaNet prefill library.
+ *
+ * The operation.  The pages name a "chunked Gated DeltaNet prefill" as one of the
+ * fused operations of their native Qwen3.5 prefill workers and test it against
+ * float64 references ("Cua-S1 4B 0.2 native text worker", kernel-test paragraph;
+ * "Open-Jev-27B-v1.1 native text worker", section "Validation and optimization
+ * scope").  They print no equations; the library computes the gated delta rule
+ * per (sequence, value head):
+ *
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   alpha_t = exp(g_t)
+ *     o_t = S_t q_t / sqrt(dk)
+ *
+ * with S a dv x dk fp32 state (S_0 = init_state, or zeros) and the last S
+ * returned as the final state.  q and k are expected to be L2-normalised per
+ * token by the caller (the pages do this in a separate fused norm operation).
+ * Internally the tokens of each sequence are processed in chunks of 64 with
+ * the WY / UT-transform form of the recurrence.
+ *
+ * Versioning.  Like the pages' library ("ABI 4", later "CUDA ABI is 5"), the
+ * ABI carries a version number; callers built against another version must be
+ * rebuilt together with the library.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+/* Status codes (0 = success, negative = error). */
+#define GDN_OK 0
+#define GDN_ERR_ARG (-1)    /* null required pointer, bad size, Hv % Hk != 0, unsupported dk/dv */
+#define GDN_ERR_ALIGN (-2)  /* a pointer is not 16-byte aligned */
+#define GDN_ERR_ALLOC (-3)  /* the library's device workspace could not be grown */
+#define GDN_ERR_LAUNCH (-4) /* a CUDA call or kernel launch failed (see gdn_last_cuda_error) */
+
+/* Returns GDN_ABI_VERSION of the loaded library. */
+int gdn_abi_version(void);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char *gdn_strerror(int status);
+
+/* The cudaError_t of the most recent GDN_ERR_LAUNCH / GDN_ERR_ALLOC on this thread (0 if none). */
+int gdn_last_cuda_error(void);
+
+/*
+ * gdn_prefill -- chunked Gated DeltaNet prefill on the GPU, asynchronous on `stream`.
+ *
+ * Pointers (all DEVICE memory, owned by the caller, not retained after return,
+ * each 16-byte aligned):
+ *   q, k        bf16 [Ttot, Hk, dk]   queries and keys (L2-normalised per token)
+ *   v           bf16 [Ttot, Hv, dv]   values
+ *   g           fp32 [Ttot, Hv]       log decay, g <= 0 (alpha = exp(g))
+ *   beta        fp32 [Ttot, Hv]       write strength in (0, 1)
+ *   cu_seqlens  int32 [B + 1] or NULL packed sequence boundaries (see below)
+ *   init_state  fp32 [B, Hv, dv, dk] or NULL (NULL = zero initial states)
+ *   out         bf16 [Ttot, Hv, dv]   outputs o_t (written; must not alias any input)
+ *   final_state fp32 [B, Hv, dv, dk] or NULL (NULL = not written); may alias init_state
+ *
+ * Sizes.  With cu_seqlens == NULL there are B sequences of T tokens each and
+ * Ttot = B * T.  Otherwise B is the number of packed sequences, sequence b covers
+ * tokens [cu_seqlens[b], cu_seqlens[b + 1]), cu_seqlens[0] = 0, cu_seqlens[B] =
+ * T = Ttot, entries non-decreasing; zero-length sequences are allowed and return
+ * their initial state.  The contents of cu_seqlens are not checked on the host
+ * (that would need a synchronisation); out-of-range entries are clamped to
+ * [0, T] on the device so no access leaves the buffers.  Value head h reads key
+ * head h / (Hv / Hk).  dk and dv must each be 32, 64 or 128.
+ *
+ * Memory.  The library keeps a per-device, grow-only workspace (allocated on the
+ * first call that needs more; about 16 KB per 64-token chunk and value head).
+ * After a call at the largest size, later calls allocate nothing.
+ *
+ * Returns GDN_OK, or an error code before anything is launched (argument and
+ * alignment errors), or GDN_ERR_LAUNCH / GDN_ERR_ALLOC.  B == 0 returns GDN_OK
+ * and does nothing.  The call does not synchronise the stream.
+ */
+int gdn_prefill(const void *q, const void *k, const void *v,
+                const float *g, const float *beta,
+                const int32_t *cu_seqlens, const float *init_state,
+                void *out, float *final_state,
+                int B, int T, int Hk, int Hv, int dk, int dv,
+                void *stream /* cudaStream_t; NULL = legacy default stream */);
+
+/*
+ * gdn_prefill_host -- the same operation on HOST buffers (same layouts; any
+ * alignment).  Copies the inputs to the library's device staging area, runs
+ * gdn_prefill on `stream`, copies out and final_state back and synchronises
+ * `stream` before returning.  Page-locked host buffers give the fastest copies.
+ * cu_seqlens, init_state and final_state may be NULL as above.
+ */
+int gdn_prefill_host(const void *q, const void *k, const void *v,
+                     const float *g, const float *beta,
+                     const int32_t *cu_seqlens, const float *init_state,
+                     void *out, float *final_state,
+                     int B, int T, int Hk, int Hv, int dk, int dv,
+                     void *stream);
+
+/*
+ * gdn_set_phase_events -- timing hook for the NEXT gdn_prefill call on this host
+ * thread.  ev_begin, ev_mid and ev_end are cudaEvent_t handles created by the
+ * caller; they are recorded on the call's stream before the chunk-preparation
+ * kernel, between it and the state-carry kernel, and after the state-carry
+ * kernel.  The hook is consumed by that one call (pass NULLs to clear it).
+ */
+void gdn_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end);
+
+/* Bytes of device workspace gdn_prefill needs for these sizes (0 on bad arguments). */
+size_t gdn_workspace_bytes(int B, int T, int Hk, int Hv, int dk, int dv, int packed);
+
+/* Release the calling device's workspace and staging buffers (synchronises the device). */
+void gdn_release_workspace(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,88 @@
+"""The C-ABI library loads and exports what include/gdn.h declares; host-side
+argument checks return their codes before any GPU work (CPU only)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from hybrid_linear_attention_prefill_gb300 import build as B
+from hybrid_linear_attention_prefill_gb300 import gdn
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return gdn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gdn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_binding_names():
+    assert sorted(gdn.EXPORTED) == declared_functions()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    raw = ctypes.CDLL(B.LIB)
+    for name in declared_functions():
+        getattr(raw, name)
+
+
+def test_abi_version_matches_header(lib):
+    m = re.search(r"#define GDN_ABI_VERSION (\d+)", open(HEADER).read())
+    assert gdn.gdn_abi_version() == int(m.group(1))
+
+
+def test_strerror(lib):
+    for code in (0, -1, -2, -3, -4, 7):
+        assert isinstance(gdn.gdn_strerror(code), str) and gdn.gdn_strerror(code)
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
+
+
+def call(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, cu_seqlens=None, init_state=None,
+             out=FAKE, final_state=None, B=1, T=64, Hk=1, Hv=1, dk=128, dv=128, stream=0)
+    a.update(kw)
+    return gdn.gdn_prefill(**a)
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(T=-5), dict(Hk=0), dict(Hv=3, Hk=2), dict(dk=48),
+                                dict(dv=256), dict(q=None), dict(out=None), dict(beta=None)])
+def test_bad_arguments_rejected(lib, kw):
+    assert call(**kw) == gdn.GDN_ERR_ARG
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "g", "beta", "out", "init_state", "final_state",
+                                  "cu_seqlens"])
+def test_misaligned_pointer_rejected(lib, name):
+    assert call(**{name: FAKE + 4}) == gdn.GDN_ERR_ALIGN
+
+
+def test_nothing_to_do(lib):
+    assert call(B=0) == gdn.GDN_OK
+    assert call(T=0) == gdn.GDN_OK  # no tokens and no final state requested
+
+
+def test_host_entry_rejects_bad_arguments(lib):
+    assert gdn.gdn_prefill_host(None, None, None, None, None, None, None, None, None,
+                                1, 4, 1, 1, 128, 128, 0) == gdn.GDN_ERR_ARG
+    assert gdn.gdn_prefill_host(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None,
+                                1, 4, 2, 3, 128, 128, 0) == gdn.GDN_ERR_ARG
+
+
+def test_workspace_bytes(lib):
+    per = 2 * 64 * 64 * 2
+    assert gdn.gdn_workspace_bytes(1, 4096, 16, 32, 128, 128, 0) == 256 + 64 * 32 * per
+    assert gdn.gdn_workspace_bytes(2, 100, 1, 1, 32, 32, 1) == 256 + (2 + 2) * per
+    assert gdn.gdn_workspace_bytes(1, 10, 2, 3, 128, 128, 0) == 0
