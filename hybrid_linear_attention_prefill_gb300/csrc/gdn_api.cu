@@ -137,6 +137,7 @@ const char* gdn_strerror(int status) {
     case GDN_ERR_ALIGN: return "pointer not 16-byte aligned";
     case GDN_ERR_ALLOC: return "device workspace allocation failed";
     case GDN_ERR_LAUNCH: return "CUDA launch or runtime call failed";
+    case GDN_ERR_SCRATCH: return "problem too large for the fixed scratch of gdn_prefill_static";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,115 @@
+// gdn_prefill_static: the prefill with its scratch in a fixed, file-scope device
+// array, for callers that cannot allocate device memory.
+//
+// Who needs this.  gdn_prefill grows a library-owned workspace with cudaMalloc
+// the first time a larger problem arrives.  Some callers cannot allow that: a
+// plugin inside an inference engine that owns all device memory and gives its
+// plugins none, code that runs with a fixed memory budget decided at start-up,
+// or a caller that must not trigger the implicit device synchronisation that
+// cudaMalloc/cudaFree bring.  This entry point takes only the caller's inputs
+// and outputs and never allocates: its scratch (the chunk table and the per-chunk
+// Tm / PT tiles) lives in `g_static_scratch` below, which every GPU that loads
+// the library holds until the process exits.
+//
+// Limits and sharing.  The array holds GDN_STATIC_SCRATCH_BYTES; a call whose
+// scratch (gdn_workspace_bytes for its sizes) does not fit returns
+// GDN_ERR_SCRATCH before launching anything.  All calls on a device share the
+// one array and it keeps the last call's contents; nothing in it has to start at
+// zero (each call writes every entry it later reads), but two calls whose work
+// overlaps on the GPU (different streams, or different host threads without
+// ordering) race on it and must be serialised by the caller.
+//
+// Set-up.  The device address of the array is looked up once per device, with
+// that device current, by the first call made on it (cudaGetSymbolAddress).
+// Make that first call before capturing a stream into a CUDA graph.
+#include <mutex>
+
+#include "../../include/gdn.h"
+#include "gdn_common.cuh"
+
+namespace gdn {
+template <int DK>
+cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
+                        void*, int, int, int, int, int, int, cudaStream_t);
+cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
+template <int DK>
+cudaError_t launch_chain(const void*, const void*, const void*, const float*, const float*, const int32_t*,
+                         const int32_t*, const void*, const float*, void*, float*, int, int, int, int, int, int,
+                         long long, cudaStream_t);
+}  // namespace gdn
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[GDN_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDev = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDev] = {};
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, const float* g,
+                                  const float* beta, const int32_t* cu_seqlens, const float* init_state,
+                                  void* out, float* final_state, int B, int T, int Hk, int Hv, int dk, int dv,
+                                  void* stream) {
+  const bool dims_ok = (dk == 32 || dk == 64 || dk == 128) && (dv == 32 || dv == 64 || dv == 128);
+  if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || Hv % Hk != 0 || !dims_ok || Hv > 65535) return GDN_ERR_ARG;
+  if ((long long)B * (dv / 32) > 0x7fffffffLL) return GDN_ERR_ARG;
+  if (B == 0) return GDN_OK;
+  const int packed = cu_seqlens != nullptr;
+  const long long ntok = packed ? (long long)T : (long long)B * T;
+  if (ntok > 0x7fffffffLL) return GDN_ERR_ARG;
+  if (ntok > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, cu_seqlens, init_state, out, final_state};
+  for (const void* p : ptrs)
+    if (p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return GDN_ERR_ALIGN;
+  if (ntok == 0 && final_state == nullptr) return GDN_OK;
+
+  // scratch layout: [chunk table, B + 1 int32, padded to 256 B][Tm/PT tiles per (slot, value head)]
+  const long long nslots = packed ? (long long)(T + gdn::kChunk - 1) / gdn::kChunk + B
+                                  : (long long)B * ((T + gdn::kChunk - 1) / gdn::kChunk);
+  const size_t table = round256(sizeof(int32_t) * ((size_t)B + 1));
+  const size_t need = table + (size_t)nslots * Hv * gdn::kWsPerSlotHead;
+  if (need > (size_t)GDN_STATIC_SCRATCH_BYTES || nslots > 0x7fffffffLL) return GDN_ERR_SCRATCH;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return GDN_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDev) return GDN_ERR_ARG;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_static_scratch);
+      if (e != cudaSuccess || p == nullptr) return GDN_ERR_LAUNCH;
+      g_static_ptr[dev] = p;
+    }
+    base = g_static_ptr[dev];
+  }
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* chunk_off = static_cast<int32_t*>(base);
+  void* tiles = static_cast<unsigned char*>(base) + table;
+  const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
+  if (packed) {
+    e = gdn::launch_chunk_table(cu_seqlens, B, T, chunk_off, st);
+    if (e != cudaSuccess) return GDN_ERR_LAUNCH;
+  }
+  if (nslots > 0) {
+    switch (dk) {
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
+    }
+    if (e != cudaSuccess) return GDN_ERR_LAUNCH;
+  }
+  switch (dk) {
+    case 32: e = gdn::launch_chain<32>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+    case 64: e = gdn::launch_chain<64>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+    default: e = gdn::launch_chain<128>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+  }
+  if (e != cudaSuccess) return GDN_ERR_LAUNCH;
+  return GDN_OK;
+}

@@ -23,10 +23,12 @@ GDN_ERR_ARG = -1
 GDN_ERR_ALIGN = -2
 GDN_ERR_ALLOC = -3
 GDN_ERR_LAUNCH = -4
+GDN_ERR_SCRATCH = -5
+GDN_STATIC_SCRATCH_BYTES = 64 << 20
 
 EXPORTED = ("gdn_abi_version", "gdn_strerror", "gdn_last_cuda_error", "gdn_prefill",
-            "gdn_prefill_host", "gdn_set_phase_events", "gdn_workspace_bytes",
-            "gdn_release_workspace")
+            "gdn_prefill_host", "gdn_prefill_static", "gdn_set_phase_events",
+            "gdn_workspace_bytes", "gdn_release_workspace")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +65,8 @@ def load(build_if_missing: bool = False):
         lib.gdn_prefill.restype = i
         lib.gdn_prefill_host.argtypes = sig
         lib.gdn_prefill_host.restype = i
+        lib.gdn_prefill_static.argtypes = sig
+        lib.gdn_prefill_static.restype = i
         lib.gdn_abi_version.argtypes = []
         lib.gdn_abi_version.restype = i
         lib.gdn_strerror.argtypes = [i]
@@ -145,6 +149,14 @@ def gdn_prefill_host(q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
     return load().gdn_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
                                    _ptr(init_state), _ptr(out), _ptr(final_state),
                                    int(B), int(T), int(Hk), int(Hv), int(dk), int(dv), _stream(stream))
+
+
+def gdn_prefill_static(q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
+                       B, T, Hk, Hv, dk, dv, stream=None) -> int:
+    """Call the allocation-free entry point (fixed device scratch); returns the status."""
+    return load().gdn_prefill_static(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                     _ptr(init_state), _ptr(out), _ptr(final_state),
+                                     int(B), int(T), int(Hk), int(Hv), int(dk), int(dv), _stream(stream))
 
 
 def check(status: int) -> None:

@@ -39,6 +39,10 @@ extern "C" {
 #define GDN_ERR_ALIGN (-2)  /* a pointer is not 16-byte aligned */
 #define GDN_ERR_ALLOC (-3)  /* the library's device workspace could not be grown */
 #define GDN_ERR_LAUNCH (-4) /* a CUDA call or kernel launch failed (see gdn_last_cuda_error) */
+#define GDN_ERR_SCRATCH (-5) /* gdn_prefill_static: the problem needs more than its fixed scratch */
+
+/* Size of the fixed device scratch array behind gdn_prefill_static (64 MiB per device). */
+#define GDN_STATIC_SCRATCH_BYTES (64u << 20)
 
 /* Returns GDN_ABI_VERSION of the loaded library. */
 int gdn_abi_version(void);
@@ -109,6 +113,34 @@ int gdn_prefill_host(const void *q, const void *k, const void *v,
  * kernel.  The hook is consumed by that one call (pass NULLs to clear it).
  */
 void gdn_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end);
+
+/*
+ * gdn_prefill_static -- gdn_prefill for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point.  It exists for callers that
+ * are not allowed to call cudaMalloc: a plugin whose host engine owns all device
+ * memory, a service with a memory budget fixed at start-up, or code that must not
+ * take the implicit device synchronisation of cudaMalloc / cudaFree.  Same
+ * arguments, layouts, alignment rules and status codes as gdn_prefill; the caller
+ * still passes the inputs and outputs.  Instead of the grow-only workspace it uses
+ * a fixed array of GDN_STATIC_SCRATCH_BYTES in device memory that every GPU
+ * loading the library holds until the process exits; it calls no allocator.
+ *   - Returns GDN_ERR_SCRATCH, before launching anything, when the problem needs
+ *     more scratch than that.  gdn_workspace_bytes gives the need: 16 KiB per
+ *     (64-token chunk, value head) pair plus a small table, so the array covers up
+ *     to 4,095 pairs -- for example one 4,096-token sequence with 32 value heads.
+ *   - All calls on a device share the array and it keeps the last call's contents.
+ *     Calls whose GPU work overlaps (other streams, other host threads) race on it:
+ *     the caller must order them.
+ *   - The first call on each device looks the array's address up (with that device
+ *     current); make that first call before capturing the stream into a CUDA graph.
+ */
+int gdn_prefill_static(const void *q, const void *k, const void *v,
+                       const float *g, const float *beta,
+                       const int32_t *cu_seqlens, const float *init_state,
+                       void *out, float *final_state,
+                       int B, int T, int Hk, int Hv, int dk, int dv,
+                       void *stream);
 
 /* Bytes of device workspace gdn_prefill needs for these sizes (0 on bad arguments). */
 size_t gdn_workspace_bytes(int B, int T, int Hk, int Hv, int dk, int dv, int packed);
