@@ -17,9 +17,9 @@ cudaError_t launch_prep(const void*, const void*, const float*, const float*, co
                         void*, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
-cudaError_t launch_chain(const void*, const void*, const void*, const float*, const float*, const int32_t*,
-                         const int32_t*, const void*, const float*, void*, float*, int, int, int, int, int, int,
-                         long long, cudaStream_t);
+cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
+                            const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
+                            int, long long, cudaStream_t);
 }  // namespace gdn
 
 namespace {
@@ -56,9 +56,10 @@ long long num_slots(int B, int T, int packed) {
   return (long long)(T + gdn::kChunk - 1) / gdn::kChunk + B;
 }
 
+// Workspace: [256 B status words][chunk table, B + 1 int32, padded to 256 B][Tm/PT tiles]
 size_t ws_bytes_for(int B, int T, int Hv, int packed) {
   const size_t table = align_up(sizeof(int32_t) * ((size_t)B + 1), 256);
-  return table + (size_t)num_slots(B, T, packed) * Hv * gdn::kWsPerSlotHead;
+  return 256 + table + (size_t)num_slots(B, T, packed) * Hv * gdn::kWsPerSlotHead;
 }
 
 int set_cuda_error(cudaError_t e, int code) {
@@ -92,8 +93,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
                const int32_t* cu, const float* init, void* out, float* fin, int B, int T, int Hk, int Hv,
                int dk, int dv, cudaStream_t st, void* ws) {
   const int packed = cu != nullptr;
-  int32_t* chunk_off = static_cast<int32_t*>(ws);
-  void* tiles = static_cast<unsigned char*>(ws) + align_up(sizeof(int32_t) * ((size_t)B + 1), 256);
+  int* err = static_cast<int*>(ws);
+  int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + 256);
+  void* tiles = static_cast<unsigned char*>(ws) + 256 + align_up(sizeof(int32_t) * ((size_t)B + 1), 256);
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   const long long nslots = num_slots(B, T, packed);
   cudaError_t e = cudaSuccess;
@@ -115,9 +117,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   }
   if (ev[1] != nullptr && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   switch (dk) {
-    case 32: e = gdn::launch_chain<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
-    case 64: e = gdn::launch_chain<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
-    default: e = gdn::launch_chain<128>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
   }
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);

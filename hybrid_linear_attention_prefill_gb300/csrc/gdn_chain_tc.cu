@@ -1,0 +1,478 @@
+// Chunk-sequential state carry on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// One CTA of 8 warps owns a 32-row slice of the dv x dk state S of one
+// (sequence, value head) and walks the sequence's 64-token chunks in order.
+// For a chunk starting from S (rows beyond the chunk's n tokens are zero,
+// with g = beta = 0), with Tm = (I + A)^-1 and PT = P Tm from the preparation
+// kernel, gamma = cumsum(g), e = exp(gamma), d = exp(gamma_last - gamma):
+//
+//   phase 1   [X; Y] = [K; Q] S^T                       (M = 128 stacked tokens, K = dk)
+//             R      = diag(beta) V - diag(beta e) X
+//   phase 2   [U; Z] = [Tm; PT] R                       (M = 128, K = 64)
+//             O      = scale (diag(e) Y + Z)            -> bf16 outputs
+//   phase 3   dS^T   = K^T diag(d) U                    (M = dk = 128, K = 64)
+//             S      = e_last S + dS
+//
+// which is the chunk form of S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T,
+// o_t = S_t q_t / sqrt(dk) (the "chunked Gated DeltaNet prefill" of the
+// "Open-Jev-27B-v1.1 native text worker" page, "Validation and optimization
+// scope").
+//
+// Latency, not arithmetic, bounds this loop: on sm_103a an MMA that accumulates
+// into the accumulator of the previous one waits ~200 cycles for it, while
+// independent MMAs issue every ~90 cycles whatever their N (up to 256).  So
+//  * the operand that carries the state in each phase (S, R, diag(d) U) is
+//    split into bf16 hi and lo parts that are stacked along N (N = 64: columns
+//    0..31 hi, 32..63 lo) instead of being issued as two MMAs, keeping the fp32
+//    state accurate to ~2^-16 at no extra MMA;
+//  * each phase splits its K dimension over independent TMEM accumulators (4 in
+//    phase 1, 2 in phases 2 and 3; 64 columns each, 256 allocated) that the
+//    epilogue adds up -- more would cost more in TMEM reads than they save.
+// A ninth warp only issues: the MMAs of each phase (ending with a tcgen05.commit
+// on an mbarrier) and the TMA loads of the next chunk (K, Q, the value slice
+// and the [Tm; PT] tile: 5-6 bulk-tensor copies into the other of two stages).
+// Epilogue warps w and w + 4 read the same 32 TMEM lanes (rows) and split the
+// 32 state columns between them.  The state S stays in fp32 registers.
+//
+// Shared-memory layouts (tile bases 1024-byte aligned):
+//   [K; Q]   K-major, 128 B swizzle: [dk/64 blocks][128 rows][128 B]; rows 0..63 K, 64..127 Q.
+//            The same K rows, read MN-major (dk contiguous), are phase 3's A operand.
+//   [Tm; PT] K-major, 128 B swizzle: [128 rows][128 B].
+//   S, R, U  MN-major, 128 B swizzle: one row per K index (d or token), 128 B =
+//            for each half of the 32 slice columns, 16 bf16 hi parts then 16 lo parts.
+//   V        the 32-column value slice, 64 B rows, 64 B swizzle.
+// TMA writes these layouts directly; out-of-range box elements (tokens past
+// the end, d >= dk) arrive as zeros.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kDVT = 32;        // state rows per CTA
+constexpr int kThreads = 288;   // 8 epilogue warps + 1 issue warp
+constexpr int kEpiThreads = 256;
+constexpr uint32_t kTmemCols = 256;
+constexpr int kParts = 4;       // independent accumulators in phase 1 (K = dk)
+constexpr int kParts23 = 2;     // and in phases 2 and 3 (K = 64)
+constexpr uint32_t kMaxPolls = 1u << 24;
+
+// stage layout (bytes)
+constexpr int kOffKQ = 0;                  // 2 x 16384
+constexpr int kOffTP = 32768;              // 16384
+constexpr int kOffV = kOffTP + 16384;      // 64 rows x 64 B (64 B swizzle)
+constexpr int kOffG = kOffV + 4096;        // 64 fp32
+constexpr int kOffB = kOffG + 256;         // 64 fp32
+constexpr int kStage = 54272;              // 53 KB, multiple of 1024
+// B operands after the two stages
+constexpr int kOffS = 2 * kStage;          // 128 rows x 128 B
+constexpr int kOffR = kOffS + 16384;       // 64 rows x 128 B
+constexpr int kOffU = kOffR + 8192;        // 64 rows x 128 B
+constexpr int kOffBar = kOffU + 8192;      // 3 MMA mbarriers, 2 load mbarriers, TMEM base, abort flag
+constexpr int kSmemBytes = kOffBar + 64 + 1024;  // + slack for 1024-byte alignment
+
+constexpr uint32_t kID_KS = tc::idesc_bf16(128, 2 * kDVT, 0, 1);  // A K-major, B MN-major
+constexpr uint32_t kID_KT = tc::idesc_bf16(128, 2 * kDVT, 1, 1);  // A MN-major, B MN-major
+
+// Write 16 fp32 values (state columns 16 cg .. 16 cg + 15) of one operand row as
+// bf16 hi parts (16-byte chunks 4 cg, 4 cg + 1) and lo parts (chunks 4 cg + 2, + 3),
+// so that accumulator columns 32 cg .. 32 cg + 31 hold this group's hi then lo sums.
+__device__ __forceinline__ void store_split16(unsigned char* tile, uint32_t row, int cg, const float (&x)[16]) {
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) split_bf16(x[2 * p], x[2 * p + 1], h[p], l[p]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, 4 * cg)) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, 4 * cg + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, 4 * cg + 2)) = make_uint4(l[0], l[1], l[2], l[3]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, 4 * cg + 3)) = make_uint4(l[4], l[5], l[6], l[7]);
+}
+
+// acc[i] = sum over the NP partial accumulators of the hi and lo products of
+// state column 16 cg + i (partial p holds columns 64 p + 32 cg ..: 16 hi, 16 lo).
+template <int NP>
+__device__ __forceinline__ void sum_parts(uint32_t taddr, int cg, float (&acc)[16]) {
+  if constexpr (NP == 2) {
+    float t[64];
+    tc::tmem_ld32x2(taddr + 32 * cg, taddr + 64 + 32 * cg, t);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = (t[i] + t[16 + i]) + (t[32 + i] + t[48 + i]);
+  } else if constexpr (NP == 4) {
+    float t[128];
+    tc::tmem_ld32x4(taddr + 32 * cg, taddr + 64 + 32 * cg, taddr + 128 + 32 * cg, taddr + 192 + 32 * cg, t);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      acc[i] = ((t[i] + t[16 + i]) + (t[32 + i] + t[48 + i])) + ((t[64 + i] + t[80 + i]) + (t[96 + i] + t[112 + i]));
+  } else {
+    float t[32];
+    tc::tmem_ld32(taddr + 32 * cg, t);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = t[i] + t[16 + i];
+#pragma unroll
+    for (int p = 1; p < NP; ++p) {
+      tc::tmem_ld32(taddr + 64 * p + 32 * cg, t);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] += t[i] + t[16 + i];
+    }
+  }
+}
+
+}  // namespace
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1)
+gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
+                    const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu,
+                    const int32_t* __restrict__ chunk_off, const float* init, __nv_bfloat16* __restrict__ out,
+                    float* fin, int* __restrict__ err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
+                    long long nslots) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
+  unsigned char* sm = smem_raw + pad;
+  const uint32_t sb = raw_s + pad;  // shared-window address of sm
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);        // [0..2] MMA phases
+  uint64_t* full = bars + 3;                                          // [0..1] stage loaded
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 40);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffBar + 44);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool issuer = warp == 8;
+  const int q4 = warp & 3;         // TMEM lane quadrant (epilogue warps)
+  const int cg = (warp >> 2) & 1;  // column group: state columns 16 cg .. 16 cg + 15
+  const int row = 32 * q4 + lane;
+  const int ntiles = DV / kDVT;
+  const int b = blockIdx.x / ntiles;
+  const int dv0 = (blockIdx.x - b * ntiles) * kDVT;
+  const int h = blockIdx.y;
+  const int hk = h / (Hv / Hk);
+  const float scale = rsqrtf((float)DK);
+  constexpr int kP1 = DK / 16 < kParts ? DK / 16 : kParts;  // partials used by phase 1
+  constexpr int kKBlocks = DK > 64 ? 2 : 1;                  // 64-wide d blocks loaded per tile
+  constexpr uint32_t kTxBytes = 2 * kKBlocks * 8192 + 4096 + 16384;
+
+  const SeqChunk sq = seq_bounds(cu, b, T);
+  const int slot0 = cu == nullptr ? b * nc_dense : chunk_off[b];
+  int nchunks = (sq.len + kChunk - 1) / kChunk;
+  if ((long long)slot0 + nchunks > nslots) nchunks = slot0 < nslots ? (int)(nslots - slot0) : 0;
+
+  // ---- set-up: TMEM, barriers, zero d-block 1 when dk <= 64 --------------------
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) tc::mbar_init(&bars[i], 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (issuer && lane == 0) {
+    tc::prefetch_tensormap(&tm_k);
+    tc::prefetch_tensormap(&tm_q);
+    tc::prefetch_tensormap(&tm_v);
+    tc::prefetch_tensormap(&tm_w);
+  }
+  if (kKBlocks == 1 && !issuer) {  // phase 3 reads all 128 rows of K^T: the rows d >= 64 stay zero
+    for (int e = tid; e < 2 * 1024; e += kEpiThreads) {
+      const int stg = e >> 10, w = e & 1023;
+      *reinterpret_cast<uint4*>(sm + stg * kStage + kOffKQ + 16384 + w * 16) = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  // ---- initial state: thread (row d, cg) holds S[16 cg + i][d] -------------------
+  const int d = row;
+  float s[16];
+  if (!issuer) {
+    const size_t base = ((size_t)b * Hv + h) * DV + dv0 + 16 * cg;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = (init != nullptr && d < DK) ? init[(base + i) * DK + d] : 0.f;
+    store_split16(sm + kOffS, d, cg, s);
+  }
+  tc::fence_proxy_async();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);  // this warp's lanes
+
+  // TMA for the tiles of chunk c into stage stg (one thread); g and beta by cp.async.
+  auto load_tiles = [&](int c, int stg) {
+    unsigned char* st = sm + stg * kStage;
+    const int t0 = (int)(sq.bos + (long long)c * kChunk);
+    tc::mbar_arrive_expect_tx(&full[stg], kTxBytes);
+#pragma unroll
+    for (int db = 0; db < kKBlocks; ++db) {
+      tc::tma_load_3d(st + kOffKQ + db * 16384, &tm_k, 64 * db, hk, t0, &full[stg]);
+      tc::tma_load_3d(st + kOffKQ + db * 16384 + 8192, &tm_q, 64 * db, hk, t0, &full[stg]);
+    }
+    tc::tma_load_3d(st + kOffV, &tm_v, dv0, h, t0, &full[stg]);
+    tc::tma_load_2d(st + kOffTP, &tm_w, 0, (int)(((long long)(slot0 + c) * Hv + h) * 128), &full[stg]);
+  };
+  auto load_scalars = [&](int c, int stg) {
+    unsigned char* st = sm + stg * kStage;
+    if (tid < kChunk) {
+      const int n = min(kChunk, sq.len - c * kChunk);
+      const bool ok = tid < n;
+      const size_t off = ok ? (size_t)(sq.bos + (long long)c * kChunk + tid) * Hv + h : 0;
+      cp_async4(st + kOffG + 4 * tid, g + off, ok);
+      cp_async4(st + kOffB + 4 * tid, beta + off, ok);
+    }
+  };
+
+  if (nchunks > 0) {
+    if (issuer && lane == 0) load_tiles(0, 0);
+    load_scalars(0, 0);
+  }
+  cp_async_commit();
+
+  const int tok = 32 * (q4 & 1) + lane;  // this thread's token in phases 1-2
+  bool aborted = false;
+  int c = 0;
+  for (; c < nchunks; ++c) {
+    const int stg = c & 1;
+    const uint32_t par = (uint32_t)(c & 1);
+    unsigned char* st = sm + stg * kStage;
+    const uint32_t st_s = sb + stg * kStage;
+    cp_async_wait<0>();
+    if (!tc::mbar_wait(&full[stg], (uint32_t)((c >> 1) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
+    __syncthreads();
+    if (*abort_flag) { aborted = true; break; }
+
+    if (issuer) {
+      // ---- phase 1: [X; Y] = [K; Q] [S_hi | S_lo]^T --------------------------------
+      if (lane == 0) {
+        tc::fence_after();
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks) {
+          const uint64_t a = tc::sdesc(st_s + kOffKQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSw128);
+          const uint64_t bd = tc::sdesc(sb + kOffS + ks * 2048, 0, 1024, tc::kSw128);
+          tc::mma_bf16(tmem + 64 * (ks & 3), a, bd, kID_KS, ks >= kParts);
+        }
+        tc::commit(&bars[0]);
+        // the other stage was last read by the previous chunk's MMAs, which are done
+        if (c + 1 < nchunks) load_tiles(c + 1, stg ^ 1);
+      }
+      __syncwarp();
+      __syncthreads();  // R written
+      if (*abort_flag) { aborted = true; break; }
+      // ---- phase 2: [U; Z] = [Tm; PT] [R_hi | R_lo] --------------------------------
+      if (lane == 0) {
+        tc::fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = tc::sdesc(st_s + kOffTP + ks * 32, 16, 1024, tc::kSw128);
+          const uint64_t bd = tc::sdesc(sb + kOffR + ks * 2048, 0, 1024, tc::kSw128);
+          tc::mma_bf16(tmem + 64 * (ks & 1), a, bd, kID_KS, ks >= kParts23);
+        }
+        tc::commit(&bars[1]);
+      }
+      __syncwarp();
+      __syncthreads();  // dU written
+      if (*abort_flag) { aborted = true; break; }
+      // ---- phase 3: dS^T = K^T [dU_hi | dU_lo] -------------------------------------
+      if (lane == 0) {
+        tc::fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = tc::sdesc(st_s + kOffKQ + ks * 2048, 16384, 1024, tc::kSw128);
+          const uint64_t bd = tc::sdesc(sb + kOffU + ks * 2048, 0, 1024, tc::kSw128);
+          tc::mma_bf16(tmem + 64 * (ks & 1), a, bd, kID_KT, ks >= kParts23);
+        }
+        tc::commit(&bars[2]);
+      }
+      __syncwarp();
+      continue;
+    }
+
+    // ================= epilogue warps =================
+    if (c + 1 < nchunks) load_scalars(c + 1, stg ^ 1);
+    cp_async_commit();
+
+    // per-token scalars: every warp scans the 64 log decays of the chunk
+    const float* gs = reinterpret_cast<const float*>(st + kOffG);
+    const float* bs = reinterpret_cast<const float*>(st + kOffB);
+    float g0 = gs[lane], g1 = gs[lane + 32];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u0 = __shfl_up_sync(0xffffffffu, g0, o);
+      const float u1 = __shfl_up_sync(0xffffffffu, g1, o);
+      if (lane >= o) { g0 += u0; g1 += u1; }
+    }
+    g1 += __shfl_sync(0xffffffffu, g0, 31);
+    const float glast = __shfl_sync(0xffffffffu, g1, 31);
+    const float gam = (q4 & 1) ? g1 : g0;
+    const float e_t = expf(gam);
+    const float d_t = expf(glast - gam);
+    const float eC = expf(glast);
+    const float b_t = bs[tok];
+
+    // ---- phase-1 epilogue: R = beta V - beta e X (rows 0..63), keep Y (rows 64..127)
+    if (!tc::mbar_wait(&bars[0], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
+    tc::fence_after();
+    float acc[16], y[16];
+    sum_parts<kP1>(tq, cg, acc);
+    if (q4 < 2) {
+      const unsigned char* vrow = st + kOffV;
+      const float be = b_t * e_t;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(vrow + tc::sw64(tok, 2 * cg + half));
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[p]));
+          const int i = 8 * half + 2 * p;
+          acc[i] = b_t * vv.x - be * acc[i];
+          acc[i + 1] = b_t * vv.y - be * acc[i + 1];
+        }
+      }
+      store_split16(sm + kOffR, tok, cg, acc);
+      tc::fence_proxy_async();  // R is read by the tensor core next
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = acc[i];
+    }
+    tc::fence_before();
+    __syncthreads();  // R written
+    if (*abort_flag) { aborted = true; break; }
+
+    // ---- phase-2 epilogue: dU (rows 0..63); outputs from Z (rows 64..127) ------------
+    if (!tc::mbar_wait(&bars[1], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
+    tc::fence_after();
+    sum_parts<kParts23>(tq, cg, acc);
+    uint32_t o8[8];
+    if (q4 < 2) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] *= d_t;
+      store_split16(sm + kOffU, tok, cg, acc);
+      tc::fence_proxy_async();  // dU is read by the tensor core next
+    } else {
+      const float es = scale * e_t;
+#pragma unroll
+      for (int p = 0; p < 8; ++p)
+        o8[p] = pack_bf16(es * y[2 * p] + scale * acc[2 * p], es * y[2 * p + 1] + scale * acc[2 * p + 1]);
+    }
+    tc::fence_before();
+    __syncthreads();  // dU written
+    if (*abort_flag) { aborted = true; break; }
+
+    // outputs go out while the phase-3 MMAs run
+    if (q4 >= 2) {
+      const int n = min(kChunk, sq.len - c * kChunk);
+      if (tok < n) {
+        __nv_bfloat16* orow =
+            out + ((size_t)(sq.bos + (long long)c * kChunk + tok) * Hv + h) * DV + dv0 + 16 * cg;
+        *reinterpret_cast<uint4*>(orow) = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+        *reinterpret_cast<uint4*>(orow + 8) = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+      }
+    }
+
+    // ---- phase-3 epilogue: S = e_last S + dS ------------------------------------------
+    if (!tc::mbar_wait(&bars[2], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
+    tc::fence_after();
+    sum_parts<kParts23>(tq, cg, acc);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = fmaf(eC, s[i], acc[i]);
+    store_split16(sm + kOffS, d, cg, s);
+    tc::fence_proxy_async();  // S is read by the tensor core at the next chunk
+    tc::fence_before();
+  }
+
+  // ---- final state, clean-up -------------------------------------------------------
+  cp_async_wait<0>();
+  if (!aborted && !issuer && fin != nullptr && d < DK) {
+    const size_t base = ((size_t)b * Hv + h) * DV + dv0 + 16 * cg;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) fin[(base + i) * DK + d] = s[i];
+  }
+  if (aborted && issuer && lane == 0) {
+    // let MMAs and TMA copies still in flight land before the CTA exits (bounded again)
+    const uint32_t par = (uint32_t)(c & 1);
+    for (int i = 0; i < 3; ++i) (void)tc::mbar_wait(&bars[i], par, 1u << 16);
+    for (int i = 0; i < 2; ++i) (void)tc::mbar_wait(&full[(c + i) & 1], (uint32_t)(((c + i) >> 1) & 1), 1u << 16);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// A bf16 tiled tensor map; dims / strides listed innermost first, strides in bytes.
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box, CUtensorMapSwizzle swz) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+template <int DK>
+cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            const int32_t* cu, const int32_t* chunk_off, const void* ws, const float* init,
+                            void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
+                            long long nslots, cudaStream_t st) {
+  const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
+  const cuuint64_t tt = (cuuint64_t)(ttot > 0 ? ttot : 1);
+  CUtensorMap mk, mq, mv, mw;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)Hk, tt};
+    const cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)Hk * DK * 2};
+    const cuuint32_t box[3] = {64, 1, 64};
+    if (!make_map(&mk, k, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mq, q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)DV, (cuuint64_t)Hv, tt};
+    const cuuint64_t strides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)Hv * DV * 2};
+    const cuuint32_t box[3] = {kDVT, 1, 64};
+    if (!make_map(&mv, v, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B)) return cudaErrorInvalidValue;
+  }
+  {
+    const long long rows = nslots * Hv * 128;
+    const cuuint64_t dims[2] = {64, (cuuint64_t)(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {64, 128};
+    if (!make_map(&mw, ws, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(gdn_chain_tc_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)B * (DV / kDVT), Hv);
+  gdn_chain_tc_kernel<DK><<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, init,
+                                                               static_cast<__nv_bfloat16*>(out), fin, err, B, T,
+                                                               Hk, Hv, DV, nc_dense, nslots);
+  return cudaGetLastError();
+}
+
+#define GDN_INST_CHAIN_TC(DK)                                                                                \
+  template cudaError_t launch_chain_tc<DK>(const void*, const void*, const void*, const float*, const float*, \
+                                           const int32_t*, const int32_t*, const void*, const float*, void*,  \
+                                           float*, int*, int, int, int, int, int, int, long long, cudaStream_t);
+GDN_INST_CHAIN_TC(32)
+GDN_INST_CHAIN_TC(64)
+GDN_INST_CHAIN_TC(128)
+
+}  // namespace gdn

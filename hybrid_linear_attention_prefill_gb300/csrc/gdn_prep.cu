@@ -16,33 +16,74 @@
 // worker" page, "Validation and optimization scope"); the WY form is the
 // standard chunked rewriting of S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T.
 //
-// One CTA handles one chunk slot and one key head, and loops over the value
-// heads that share the key head, so the Grams K K^T and Q K^T are computed once
-// per key head.  Only non-positive exponents are ever taken (gamma_t - gamma_i,
-// i <= t), so nothing overflows however strong the decay.
+// One CTA (8 warps) handles one chunk slot and one key head, and loops over the
+// value heads that share the key head, so the Grams K K^T and Q K^T are computed
+// once per key head.  The inverse is blocked: the four 16 x 16 diagonal blocks
+// by forward substitution in fp32, then the 16 -> 32 -> 64 merges
+// T21 = -T22 A21 T11 as tensor-core products whose fp32 operands are split into
+// bf16 hi + lo parts (hi*hi + hi*lo + lo*hi, ~2^-16 relative).  Only non-positive
+// exponents are ever taken (gamma_t - gamma_i, i <= t), so nothing overflows
+// however strong the decay.
 #include "gdn_common.cuh"
 
 namespace gdn {
 
+namespace {
+
+constexpr int kPrepThreads = 256;
+constexpr int LDF = 68;  // fp32 row stride of 64-wide matrices
+constexpr int LDB = 72;  // bf16 row stride of 64-wide matrices
+constexpr int LDW = 36;  // fp32 row stride of the 32-wide merge buffer
+
+// acc (16 x 8 tile) += X[r0:r0+16, k0:k0+16] * Y[ky:ky+16, n0:n0+8] for fp32 X, Y in
+// shared memory, as three bf16 products of the hi / lo splits.
+__device__ __forceinline__ void mma_f32x3(float (&acc)[4], const float* X, int ldx, int r0, int k0,
+                                          const float* Y, int ldy, int ky, int n0, int lane) {
+  const int g8 = lane >> 2, tg = lane & 3;
+  const float2 x0 = *reinterpret_cast<const float2*>(X + (r0 + g8) * ldx + k0 + 2 * tg);
+  const float2 x1 = *reinterpret_cast<const float2*>(X + (r0 + g8 + 8) * ldx + k0 + 2 * tg);
+  const float2 x2 = *reinterpret_cast<const float2*>(X + (r0 + g8) * ldx + k0 + 8 + 2 * tg);
+  const float2 x3 = *reinterpret_cast<const float2*>(X + (r0 + g8 + 8) * ldx + k0 + 8 + 2 * tg);
+  uint32_t ah[4], al[4];
+  split_bf16(x0.x, x0.y, ah[0], al[0]);
+  split_bf16(x1.x, x1.y, ah[1], al[1]);
+  split_bf16(x2.x, x2.y, ah[2], al[2]);
+  split_bf16(x3.x, x3.y, ah[3], al[3]);
+  uint32_t bh0, bl0, bh1, bl1;
+  split_bf16(Y[(ky + 2 * tg) * ldy + n0 + g8], Y[(ky + 2 * tg + 1) * ldy + n0 + g8], bh0, bl0);
+  split_bf16(Y[(ky + 2 * tg + 8) * ldy + n0 + g8], Y[(ky + 2 * tg + 9) * ldy + n0 + g8], bh1, bl1);
+  mma_bf16(acc, ah, bh0, bh1);
+  mma_bf16(acc, ah, bl0, bl1);
+  mma_bf16(acc, al, bh0, bh1);
+}
+
+// Store a 16 x 8 accumulator tile (times `sgn`) at D[r0.., n0..].
+__device__ __forceinline__ void store_tile(float* D, int ldd, int r0, int n0, const float (&acc)[4], float sgn,
+                                           int lane) {
+  const int g8 = lane >> 2, tg = lane & 3;
+  *reinterpret_cast<float2*>(D + (r0 + g8) * ldd + n0 + 2 * tg) = make_float2(sgn * acc[0], sgn * acc[1]);
+  *reinterpret_cast<float2*>(D + (r0 + g8 + 8) * ldd + n0 + 2 * tg) = make_float2(sgn * acc[2], sgn * acc[3]);
+}
+
+}  // namespace
+
 template <int DK>
 struct PrepSmem {
   static constexpr int LDK = DK + 8;  // bf16 row stride of the K/Q tiles (conflict-free ldmatrix)
-  static constexpr int LDF = 68;      // fp32 row stride of 64-wide matrices
-  static constexpr int LDB = 72;      // bf16 row stride of 64-wide matrices
   static constexpr int kKQBytes = 2 * kChunk * LDK * 2;
   static constexpr int kATBytes = 2 * kChunk * LDF * 4;
   static constexpr int kUnion = kKQBytes > kATBytes ? kKQBytes : kATBytes;
-  // [union: K,Q tiles | A,Tm fp32] [G fp32 x2] [P bf16] [Tm bf16] [W temp] [gamma, beta]
+  // [union: K,Q tiles | A,Tm fp32] [G fp32 x2] [P bf16] [Tm bf16] [merge buffer] [gamma, beta]
   static constexpr int offG = kUnion;
   static constexpr int offP = offG + 2 * kChunk * LDF * 4;
   static constexpr int offTb = offP + kChunk * LDB * 2;
   static constexpr int offW = offTb + kChunk * LDB * 2;
-  static constexpr int offGam = offW + 3 * 16 * 17 * 4;
+  static constexpr int offGam = offW + 32 * LDW * 4;
   static constexpr int bytes = offGam + 2 * kChunk * 4;
 };
 
 template <int DK>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kPrepThreads, 2)
 gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                 const float* __restrict__ g, const float* __restrict__ beta,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_off,
@@ -51,12 +92,12 @@ gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   extern __shared__ __align__(128) unsigned char smem[];
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem);
   __nv_bfloat16* Qs = Ks + kChunk * L::LDK;
-  float* As = reinterpret_cast<float*>(smem);     // aliases K/Q after the Grams
-  float* Tms = As + kChunk * L::LDF;
+  float* As = reinterpret_cast<float*>(smem);  // aliases K/Q after the Grams
+  float* Tms = As + kChunk * LDF;
   float* Gs = reinterpret_cast<float*>(smem + L::offG);  // [2][64][LDF]
   __nv_bfloat16* Ps = reinterpret_cast<__nv_bfloat16*>(smem + L::offP);
   __nv_bfloat16* Tmb = reinterpret_cast<__nv_bfloat16*>(smem + L::offTb);
-  float* Wt = reinterpret_cast<float*>(smem + L::offW);  // [3][16][17]
+  float* Wt = reinterpret_cast<float*>(smem + L::offW);  // [32][LDW]
   float* gam = reinterpret_cast<float*>(smem + L::offGam);
   float* bet = gam + kChunk;
 
@@ -73,7 +114,7 @@ gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     if (slot >= chunk_off[B]) return;
     int lo = 0, hi = B;  // largest b with chunk_off[b] <= slot
     while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
+      const int mid = (lo + hi) >> 1;
       if (chunk_off[mid] <= slot) lo = mid; else hi = mid;
     }
     b = lo;
@@ -86,7 +127,7 @@ gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   // ---- load the K and Q tiles (rows >= n are zero) ---------------------------
   {
     constexpr int CPR = DK / 8;  // 16-byte pieces per row
-    for (int e = tid; e < kChunk * CPR; e += 128) {
+    for (int e = tid; e < kChunk * CPR; e += kPrepThreads) {
       const int r = e / CPR, p = e - r * CPR;
       const bool ok = r < n;
       const size_t off = ok ? ((size_t)(t0 + r) * Hk + hk) * DK + p * 8 : 0;
@@ -100,40 +141,30 @@ gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
 
   // ---- Grams: G0 = K K^T, G1 = Q K^T on the lower block triangle ------------
   {
-    const int mat = warp >> 1;
+    const int mat = warp >> 2, mi = warp & 3;
     const __nv_bfloat16* Asrc = mat == 0 ? Ks : Qs;
-    float* Gd = Gs + mat * kChunk * L::LDF;
+    float* Gd = Gs + mat * kChunk * LDF;
     const int m = lane >> 3;
+    float acc[8][4];
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int mi = (warp & 1) == 0 ? (s == 0 ? 0 : 3) : (s == 0 ? 1 : 2);
-      float acc[8][4];
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int kk = 0; kk < DK / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(a, Asrc + (16 * mi + 8 * (m & 1) + (lane & 7)) * L::LDK + 16 * kk + 8 * (m >> 1));
 #pragma unroll
-      for (int kk = 0; kk < DK / 16; ++kk) {
-        uint32_t a[4];
-        ldsm_x4(a, Asrc + (16 * mi + 8 * (m & 1) + (lane & 7)) * L::LDK + 16 * kk + 8 * (m >> 1));
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          if (p <= mi) {
-            uint32_t bb[4];
-            ldsm_x4(bb, Ks + (8 * (2 * p + (m >> 1)) + (lane & 7)) * L::LDK + 16 * kk + 8 * (m & 1));
-            mma_bf16(acc[2 * p], a, bb[0], bb[1]);
-            mma_bf16(acc[2 * p + 1], a, bb[2], bb[3]);
-          }
-        }
-      }
-      const int r0 = 16 * mi + (lane >> 2);
-#pragma unroll
-      for (int nj = 0; nj < 8; ++nj) {
-        if (nj <= 2 * mi + 1) {
-          const int cc = 8 * nj + 2 * (lane & 3);
-          *reinterpret_cast<float2*>(Gd + r0 * L::LDF + cc) = make_float2(acc[nj][0], acc[nj][1]);
-          *reinterpret_cast<float2*>(Gd + (r0 + 8) * L::LDF + cc) = make_float2(acc[nj][2], acc[nj][3]);
+      for (int p = 0; p < 4; ++p) {
+        if (p <= mi) {
+          uint32_t bb[4];
+          ldsm_x4(bb, Ks + (8 * (2 * p + (m >> 1)) + (lane & 7)) * L::LDK + 16 * kk + 8 * (m & 1));
+          mma_bf16(acc[2 * p], a, bb[0], bb[1]);
+          mma_bf16(acc[2 * p + 1], a, bb[2], bb[3]);
         }
       }
     }
+#pragma unroll
+    for (int nj = 0; nj < 8; ++nj)
+      if (nj <= 2 * mi + 1) store_tile(Gd, LDF, 16 * mi, 8 * nj, acc[nj], 1.f, lane);
   }
   __syncthreads();
 
@@ -159,31 +190,25 @@ gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     }
     __syncthreads();
 
-    // ---- A (fp32) and P (bf16) -------------------------------------------------
-    for (int e = tid; e < kChunk * kChunk; e += 128) {
+    // ---- A (fp32), P (bf16); zero the blocks of Tm above the diagonal --------
+    for (int e = tid; e < kChunk * kChunk; e += kPrepThreads) {
       const int t = e >> 6, i = e & 63;
       float a = 0.f, p = 0.f;
       if (i <= t) {
-        const float d = expf(gam[t] - gam[i]);
-        p = d * Gs[kChunk * L::LDF + t * L::LDF + i];
-        if (i < t) a = bet[t] * d * Gs[t * L::LDF + i];
+        const float dcy = expf(gam[t] - gam[i]);
+        p = dcy * Gs[kChunk * LDF + t * LDF + i];
+        if (i < t) a = bet[t] * dcy * Gs[t * LDF + i];
       }
-      As[t * L::LDF + i] = a;
-      Ps[t * L::LDB + i] = __float2bfloat16_rn(p);
-    }
-    // zero the strictly-upper 16x16 blocks of Tm
-    for (int e = tid; e < 6 * 256; e += 128) {
-      const int blk = e >> 8, w = e & 255;
-      const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-      const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      Tms[(16 * bi + (w >> 4)) * L::LDF + 16 * bj + (w & 15)] = 0.f;
+      As[t * LDF + i] = a;
+      Ps[t * LDB + i] = __float2bfloat16_rn(p);
+      if ((i >> 4) > (t >> 4)) Tms[t * LDF + i] = 0.f;
     }
     __syncthreads();
 
-    // ---- Tm = (I + A)^-1: diagonal 16x16 blocks by forward substitution ------
+    // ---- Tm: the four 16 x 16 diagonal blocks by forward substitution --------
     if (tid < 64) {
       const int blk = tid >> 4, j = tid & 15;
-      const float* Ab = As + 16 * blk * L::LDF + 16 * blk;
+      const float* Ab = As + 16 * blk * LDF + 16 * blk;
       float x[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
@@ -191,94 +216,108 @@ gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       for (int t = 1; t < 16; ++t) {
         float s = 0.f;
 #pragma unroll
-        for (int i = 0; i < t; ++i) s = fmaf(Ab[t * L::LDF + i], x[i], s);
+        for (int i = 0; i < t; ++i) s = fmaf(Ab[t * LDF + i], x[i], s);
         if (t > j) x[t] = -s;
       }
-      float* Tb = Tms + 16 * blk * L::LDF + 16 * blk;
+      float* Tb = Tms + 16 * blk * LDF + 16 * blk;
 #pragma unroll
-      for (int t = 0; t < 16; ++t) Tb[t * L::LDF + j] = x[t];
+      for (int t = 0; t < 16; ++t) Tb[t * LDF + j] = x[t];
     }
     __syncthreads();
-    // ---- off-diagonal blocks, one block row at a time ------------------------
-    //   Tm_ij = -Tm_ii * sum_{kb=j}^{i-1} A_{i,kb} Tm_{kb,j}
-    for (int bi = 1; bi < 4; ++bi) {
-      for (int e = tid; e < bi * 256; e += 128) {
-        const int bj = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-        const float* Ar = As + (16 * bi + r) * L::LDF;
-        float s = 0.f;
-        for (int kb = bj; kb < bi; ++kb) {
+
+    // ---- merge 16 -> 32: T[o+16.., o..] = -T22 (A21 T11), o = 0 and 32 -------
+    if (warp < 2) {
+      const int o = 32 * warp;
+      float* W = Wt + 16 * warp * LDW;  // this warp's 16 x 16 part of the buffer
 #pragma unroll
-          for (int mm = 0; mm < 16; ++mm)
-            s = fmaf(Ar[16 * kb + mm], Tms[(16 * kb + mm) * L::LDF + 16 * bj + cc], s);
-        }
-        Wt[(bj * 16 + r) * 17 + cc] = s;
+      for (int nt = 0; nt < 2; ++nt) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f32x3(acc, As, LDF, o + 16, o, Tms, LDF, o, o + 8 * nt, lane);
+        store_tile(W, LDW, 0, 8 * nt, acc, 1.f, lane);
       }
-      __syncthreads();
-      for (int e = tid; e < bi * 256; e += 128) {
-        const int bj = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-        const float* Tr = Tms + (16 * bi + r) * L::LDF + 16 * bi;
-        float s = 0.f;
+      __syncwarp();
 #pragma unroll
-        for (int mm = 0; mm < 16; ++mm)
-          if (mm <= r) s = fmaf(Tr[mm], Wt[(bj * 16 + mm) * 17 + cc], s);
-        Tms[(16 * bi + r) * L::LDF + 16 * bj + cc] = -s;
+      for (int nt = 0; nt < 2; ++nt) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f32x3(acc, Tms, LDF, o + 16, o + 16, W, LDW, 0, 8 * nt, lane);
+        store_tile(Tms, LDF, o + 16, o + 8 * nt, acc, -1.f, lane);
       }
-      __syncthreads();
     }
+    __syncthreads();
+
+    // ---- merge 32 -> 64: T[32.., 0..32] = -T[32..,32..] (A[32..,0..32] T[0..32,0..32]) ----
+    {
+      const int mt = warp >> 2, nt = warp & 3;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) mma_f32x3(acc, As, LDF, 32 + 16 * mt, 16 * kk, Tms, LDF, 16 * kk, 8 * nt, lane);
+      store_tile(Wt, LDW, 16 * mt, 8 * nt, acc, 1.f, lane);
+      __syncthreads();
+      float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+        mma_f32x3(acc2, Tms, LDF, 32 + 16 * mt, 32 + 16 * kk, Wt, LDW, 16 * kk, 8 * nt, lane);
+      store_tile(Tms, LDF, 32 + 16 * mt, 8 * nt, acc2, -1.f, lane);
+    }
+    __syncthreads();
 
     // ---- bf16 Tm: to shared (for PT) and to the workspace ---------------------
     __nv_bfloat16* wsT = ws + ((size_t)slot * Hv + h) * (2 * kWsTileElems);
     __nv_bfloat16* wsPT = wsT + kWsTileElems;
-    for (int e = tid; e < kChunk * 8; e += 128) {
+    for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
       const int r = e >> 3, p = e & 7;
-      const float* src = Tms + r * L::LDF + 8 * p;
+      const float* src = Tms + r * LDF + 8 * p;
       uint4 v;
       v.x = pack_bf16(src[0], src[1]);
       v.y = pack_bf16(src[2], src[3]);
       v.z = pack_bf16(src[4], src[5]);
       v.w = pack_bf16(src[6], src[7]);
-      *reinterpret_cast<uint4*>(Tmb + r * L::LDB + 8 * p) = v;
+      *reinterpret_cast<uint4*>(Tmb + r * LDB + 8 * p) = v;
       *reinterpret_cast<uint4*>(wsT + r * kChunk + 8 * p) = v;
     }
     __syncthreads();
 
-    // ---- PT = P Tm (lower triangular); warp w owns rows 16w..16w+15 ----------
+    // ---- PT = P Tm (lower triangular); warp w: rows 16 (w/2).., column pairs ---
     {
-      const int m = lane >> 3;
-      float acc[8][4];
+      const int mi = warp >> 1, m = lane >> 3;
+      float acc[4][4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        if (kk <= warp) {
+        if (kk <= mi) {
           uint32_t a[4];
-          ldsm_x4(a, Ps + (16 * warp + 8 * (m & 1) + (lane & 7)) * L::LDB + 16 * kk + 8 * (m >> 1));
+          ldsm_x4(a, Ps + (16 * mi + 8 * (m & 1) + (lane & 7)) * LDB + 16 * kk + 8 * (m >> 1));
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            if (p <= kk) {  // columns j < 16(kk+1) only
+          for (int pp = 0; pp < 2; ++pp) {
+            const int p = 2 * (warp & 1) + pp;  // column pair: columns 16 p .. 16 p + 15
+            if (p <= kk) {
               uint32_t bb[4];
-              ldsm_x4_t(bb, Tmb + (16 * kk + 8 * (m & 1) + (lane & 7)) * L::LDB + 8 * (2 * p + (m >> 1)));
-              mma_bf16(acc[2 * p], a, bb[0], bb[1]);
-              mma_bf16(acc[2 * p + 1], a, bb[2], bb[3]);
+              ldsm_x4_t(bb, Tmb + (16 * kk + 8 * (m & 1) + (lane & 7)) * LDB + 8 * (2 * p + (m >> 1)));
+              mma_bf16(acc[2 * pp], a, bb[0], bb[1]);
+              mma_bf16(acc[2 * pp + 1], a, bb[2], bb[3]);
             }
           }
         }
       }
-      __syncwarp();
-      // each warp overwrites only its own rows of Ps, which only it reads
-      const int r0 = 16 * warp + (lane >> 2);
+      __syncthreads();  // every warp has read P before it is overwritten with PT
+      const int r0 = 16 * mi + (lane >> 2);
 #pragma unroll
-      for (int nj = 0; nj < 8; ++nj) {
-        const int cc = 8 * nj + 2 * (lane & 3);
-        *reinterpret_cast<uint32_t*>(Ps + r0 * L::LDB + cc) = pack_bf16(acc[nj][0], acc[nj][1]);
-        *reinterpret_cast<uint32_t*>(Ps + (r0 + 8) * L::LDB + cc) = pack_bf16(acc[nj][2], acc[nj][3]);
+      for (int pp = 0; pp < 2; ++pp) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int cc = 16 * (2 * (warp & 1) + pp) + 8 * hh + 2 * (lane & 3);
+          *reinterpret_cast<uint32_t*>(Ps + r0 * LDB + cc) = pack_bf16(acc[2 * pp + hh][0], acc[2 * pp + hh][1]);
+          *reinterpret_cast<uint32_t*>(Ps + (r0 + 8) * LDB + cc) =
+              pack_bf16(acc[2 * pp + hh][2], acc[2 * pp + hh][3]);
+        }
       }
     }
     __syncthreads();
-    for (int e = tid; e < kChunk * 8; e += 128) {
+    for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
       const int r = e >> 3, p = e & 7;
       *reinterpret_cast<uint4*>(wsPT + r * kChunk + 8 * p) =
-          *reinterpret_cast<const uint4*>(Ps + r * L::LDB + 8 * p);
+          *reinterpret_cast<const uint4*>(Ps + r * LDB + 8 * p);
     }
     __syncthreads();
   }
@@ -336,7 +375,7 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   cudaError_t e = cudaFuncSetAttribute(gdn_prep_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::bytes);
   if (e != cudaSuccess) return e;
   dim3 grid(nslots, Hk);
-  gdn_prep_kernel<DK><<<grid, 128, L::bytes, st>>>(
+  gdn_prep_kernel<DK><<<grid, kPrepThreads, L::bytes, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g, beta, cu, chunk_off,
       static_cast<__nv_bfloat16*>(ws), B, T, Hk, Hv, nc_dense);
   return cudaGetLastError();

@@ -33,9 +33,9 @@ cudaError_t launch_prep(const void*, const void*, const float*, const float*, co
                         void*, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
-cudaError_t launch_chain(const void*, const void*, const void*, const float*, const float*, const int32_t*,
-                         const int32_t*, const void*, const float*, void*, float*, int, int, int, int, int, int,
-                         long long, cudaStream_t);
+cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
+                            const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
+                            int, long long, cudaStream_t);
 }  // namespace gdn
 
 namespace {
@@ -66,11 +66,11 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
     if (p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return GDN_ERR_ALIGN;
   if (ntok == 0 && final_state == nullptr) return GDN_OK;
 
-  // scratch layout: [chunk table, B + 1 int32, padded to 256 B][Tm/PT tiles per (slot, value head)]
+  // scratch layout: [256 B status words][chunk table, B + 1 int32, padded to 256 B][Tm/PT tiles]
   const long long nslots = packed ? (long long)(T + gdn::kChunk - 1) / gdn::kChunk + B
                                   : (long long)B * ((T + gdn::kChunk - 1) / gdn::kChunk);
   const size_t table = round256(sizeof(int32_t) * ((size_t)B + 1));
-  const size_t need = table + (size_t)nslots * Hv * gdn::kWsPerSlotHead;
+  const size_t need = 256 + table + (size_t)nslots * Hv * gdn::kWsPerSlotHead;
   if (need > (size_t)GDN_STATIC_SCRATCH_BYTES || nslots > 0x7fffffffLL) return GDN_ERR_SCRATCH;
 
   int dev = 0;
@@ -90,8 +90,9 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int32_t* chunk_off = static_cast<int32_t*>(base);
-  void* tiles = static_cast<unsigned char*>(base) + table;
+  int* err = static_cast<int*>(base);
+  int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + 256);
+  void* tiles = static_cast<unsigned char*>(base) + 256 + table;
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   if (packed) {
     e = gdn::launch_chunk_table(cu_seqlens, B, T, chunk_off, st);
@@ -106,9 +107,9 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
     if (e != cudaSuccess) return GDN_ERR_LAUNCH;
   }
   switch (dk) {
-    case 32: e = gdn::launch_chain<32>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
-    case 64: e = gdn::launch_chain<64>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
-    default: e = gdn::launch_chain<128>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
   }
   if (e != cudaSuccess) return GDN_ERR_LAUNCH;
   return GDN_OK;
