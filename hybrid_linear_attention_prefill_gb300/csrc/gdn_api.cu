@@ -14,7 +14,7 @@
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, int, int, int, int, int, int, cudaStream_t);
+                        void*, int*, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
@@ -109,9 +109,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   if (nslots > 0) {
     if (nslots > 0x7fffffffLL) return GDN_ERR_ARG;
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
     }
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }

@@ -24,7 +24,10 @@
 // bf16 hi + lo parts (hi*hi + hi*lo + lo*hi, ~2^-16 relative).  Only non-positive
 // exponents are ever taken (gamma_t - gamma_i, i <= t), so nothing overflows
 // however strong the decay.
-#include "gdn_common.cuh"
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "gdn_tc.cuh"
 
 namespace gdn {
 
@@ -69,29 +72,32 @@ __device__ __forceinline__ void store_tile(float* D, int ldd, int r0, int n0, co
 
 template <int DK>
 struct PrepSmem {
-  static constexpr int LDK = DK + 8;  // bf16 row stride of the K/Q tiles (conflict-free ldmatrix)
-  static constexpr int kKQBytes = 2 * kChunk * LDK * 2;
+  // [union: K,Q tiles (TMA, 128 B swizzle) | A,Tm fp32] [G fp32 x2] [P bf16] [Tm bf16] [merge buffer]
+  // [gamma, beta] [mbarrier]
+  static constexpr int kKQBytes = 32768;
   static constexpr int kATBytes = 2 * kChunk * LDF * 4;
   static constexpr int kUnion = kKQBytes > kATBytes ? kKQBytes : kATBytes;
-  // [union: K,Q tiles | A,Tm fp32] [G fp32 x2] [P bf16] [Tm bf16] [merge buffer] [gamma, beta]
   static constexpr int offG = kUnion;
   static constexpr int offP = offG + 2 * kChunk * LDF * 4;
   static constexpr int offTb = offP + kChunk * LDB * 2;
   static constexpr int offW = offTb + kChunk * LDB * 2;
   static constexpr int offGam = offW + 32 * LDW * 4;
-  static constexpr int bytes = offGam + 2 * kChunk * 4;
+  static constexpr int offBar = offGam + 2 * kChunk * 4;
+  static constexpr int bytes = offBar + 16 + 1024;  // + slack for 1024-byte alignment
 };
 
 template <int DK>
 __global__ void __launch_bounds__(kPrepThreads, 2)
-gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                 const float* __restrict__ g, const float* __restrict__ beta,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_off,
-                __nv_bfloat16* __restrict__ ws, int B, int T, int Hk, int Hv, int nc_dense) {
+                __nv_bfloat16* __restrict__ ws, int* __restrict__ err, int B, int T, int Hk, int Hv,
+                int nc_dense) {
   using L = PrepSmem<DK>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem);
-  __nv_bfloat16* Qs = Ks + kChunk * L::LDK;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  unsigned char* KQ = smem;                    // [2][128][128 B], swizzled
   float* As = reinterpret_cast<float*>(smem);  // aliases K/Q after the Grams
   float* Tms = As + kChunk * LDF;
   float* Gs = reinterpret_cast<float*>(smem + L::offG);  // [2][64][LDF]
@@ -100,6 +106,7 @@ gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   float* Wt = reinterpret_cast<float*>(smem + L::offW);  // [32][LDW]
   float* gam = reinterpret_cast<float*>(smem + L::offGam);
   float* bet = gam + kChunk;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::offBar);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = blockIdx.x, hk = blockIdx.y;
@@ -124,49 +131,95 @@ gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   const long long t0 = sq.bos + (long long)c * kChunk;
   const int n = min(kChunk, sq.len - c * kChunk);
 
-  // ---- load the K and Q tiles (rows >= n are zero) ---------------------------
-  {
-    constexpr int CPR = DK / 8;  // 16-byte pieces per row
-    for (int e = tid; e < kChunk * CPR; e += kPrepThreads) {
-      const int r = e / CPR, p = e - r * CPR;
-      const bool ok = r < n;
-      const size_t off = ok ? ((size_t)(t0 + r) * Hk + hk) * DK + p * 8 : 0;
-      cp_async16(Ks + r * L::LDK + p * 8, k + off, ok);
-      cp_async16(Qs + r * L::LDK + p * 8, q + off, ok);
+  // ---- load the K and Q tiles by TMA (tokens past the end of the tensor are zero)
+  constexpr int kKBlocks = DK > 64 ? 2 : 1;
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_mbar_init();
+    tc::mbar_arrive_expect_tx(bar, 2 * kKBlocks * 8192);
+#pragma unroll
+    for (int db = 0; db < kKBlocks; ++db) {
+      tc::tma_load_3d(KQ + db * 16384, &tm_k, 64 * db, hk, (int)t0, bar);
+      tc::tma_load_3d(KQ + db * 16384 + 8192, &tm_q, 64 * db, hk, (int)t0, bar);
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
   }
+  __syncthreads();
+  if (!tc::mbar_wait(bar, 0, 1u << 24)) atomicOr(err, 4);
+  // rows t >= n belong to the next sequence (or are past the end): clear them
+  if (n < kChunk) {
+    for (int e = tid; e < kKBlocks * 2 * (kChunk - n) * 8; e += kPrepThreads) {
+      const int piece = e & 7, rr = e >> 3;
+      const int r = n + rr % (kChunk - n), which = (rr / (kChunk - n)) & 1, db = rr / (2 * (kChunk - n));
+      *reinterpret_cast<uint4*>(KQ + db * 16384 + tc::sw128(64 * which + r, piece)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  __syncthreads();
 
   // ---- Grams: G0 = K K^T, G1 = Q K^T on the lower block triangle ------------
+  // Warp roles: matrix (K or Q rows), m-tile pair {0,3} or {1,2} (10 n-tiles each),
+  // and which half of the dk range; the second half is added into the first.
   {
-    const int mat = warp >> 2, mi = warp & 3;
-    const __nv_bfloat16* Asrc = mat == 0 ? Ks : Qs;
+    const int mat = warp & 1, pairsel = (warp >> 1) & 1, khalf = warp >> 2;
     float* Gd = Gs + mat * kChunk * LDF;
     const int m = lane >> 3;
-    float acc[8][4];
+    constexpr int KS = DK / 16;
+    constexpr int KH = KS / 2 > 0 ? KS / 2 : 1;
+    float acc[2][8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int u = 0; u < 2; ++u)
 #pragma unroll
-    for (int kk = 0; kk < DK / 16; ++kk) {
-      uint32_t a[4];
-      ldsm_x4(a, Asrc + (16 * mi + 8 * (m & 1) + (lane & 7)) * L::LDK + 16 * kk + 8 * (m >> 1));
+      for (int i = 0; i < 8; ++i) acc[u][i][0] = acc[u][i][1] = acc[u][i][2] = acc[u][i][3] = 0.f;
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        if (p <= mi) {
-          uint32_t bb[4];
-          ldsm_x4(bb, Ks + (8 * (2 * p + (m >> 1)) + (lane & 7)) * L::LDK + 16 * kk + 8 * (m & 1));
-          mma_bf16(acc[2 * p], a, bb[0], bb[1]);
-          mma_bf16(acc[2 * p + 1], a, bb[2], bb[3]);
+    for (int kq = 0; kq < KH; ++kq) {
+      const int kk = khalf * KH + kq;
+      if (kk < KS) {
+        const int db = kk >> 2, c0 = 2 * (kk & 3);  // 16-byte piece of the 128 B row
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int mi = pairsel == 0 ? (u == 0 ? 0 : 3) : (u == 0 ? 1 : 2);
+          uint32_t a[4];
+          const int ra = 64 * mat + 16 * mi + 8 * (m & 1) + (lane & 7);
+          ldsm_x4(a, KQ + db * 16384 + tc::sw128(ra, c0 + (m >> 1)));
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            if (p <= mi) {
+              uint32_t bb[4];
+              const int rb = 8 * (2 * p + (m >> 1)) + (lane & 7);
+              ldsm_x4(bb, KQ + db * 16384 + tc::sw128(rb, c0 + (m & 1)));
+              mma_bf16(acc[u][2 * p], a, bb[0], bb[1]);
+              mma_bf16(acc[u][2 * p + 1], a, bb[2], bb[3]);
+            }
+          }
         }
       }
     }
+    // first k half stores, second k half adds
 #pragma unroll
-    for (int nj = 0; nj < 8; ++nj)
-      if (nj <= 2 * mi + 1) store_tile(Gd, LDF, 16 * mi, 8 * nj, acc[nj], 1.f, lane);
+    for (int phase = 0; phase < 2; ++phase) {
+      if (phase == khalf) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int mi = pairsel == 0 ? (u == 0 ? 0 : 3) : (u == 0 ? 1 : 2);
+#pragma unroll
+          for (int nj = 0; nj < 8; ++nj) {
+            if (nj <= 2 * mi + 1) {
+              const int g8 = lane >> 2, tg = lane & 3;
+              float* d0 = Gd + (16 * mi + g8) * LDF + 8 * nj + 2 * tg;
+              float* d1 = d0 + 8 * LDF;
+              if (phase == 0) {
+                *reinterpret_cast<float2*>(d0) = make_float2(acc[u][nj][0], acc[u][nj][1]);
+                *reinterpret_cast<float2*>(d1) = make_float2(acc[u][nj][2], acc[u][nj][3]);
+              } else {
+                d0[0] += acc[u][nj][0]; d0[1] += acc[u][nj][1];
+                d1[0] += acc[u][nj][2]; d1[1] += acc[u][nj][3];
+              }
+            }
+          }
+        }
+      }
+      __syncthreads();
+    }
   }
-  __syncthreads();
 
   const int G = Hv / Hk;
   for (int gi = 0; gi < G; ++gi) {
@@ -183,42 +236,65 @@ gdn_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         if (lane >= o) { g0 += u0; g1 += u1; }
       }
       g1 += __shfl_sync(0xffffffffu, g0, 31);
-      gam[lane] = g0;
-      gam[lane + 32] = g1;
+      gam[lane] = g0 * 1.4426950408889634f;  // log2(e)
+      gam[lane + 32] = g1 * 1.4426950408889634f;
       bet[lane] = b0;
       bet[lane + 32] = b1;
     }
     __syncthreads();
 
-    // ---- A (fp32), P (bf16); zero the blocks of Tm above the diagonal --------
-    for (int e = tid; e < kChunk * kChunk; e += kPrepThreads) {
-      const int t = e >> 6, i = e & 63;
-      float a = 0.f, p = 0.f;
-      if (i <= t) {
-        const float dcy = expf(gam[t] - gam[i]);
-        p = dcy * Gs[kChunk * LDF + t * LDF + i];
-        if (i < t) a = bet[t] * dcy * Gs[t * LDF + i];
+    // ---- A (fp32) and P (bf16), 8 columns at a time, lower triangle only ----------
+    // Gamma[t][i] = 2^(gamma2_t - gamma2_i) with gamma2 = gamma log2(e): the exponent
+    // is never positive for i <= t.
+    for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
+      const int t = e >> 3, c8 = (e & 7) * 8;
+      float av[8], pv[8];
+      if (c8 <= t) {
+        const float gt = gam[t], bt = bet[t];
+        const float* gk = Gs + t * LDF + c8;
+        const float* gq = Gs + kChunk * LDF + t * LDF + c8;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = c8 + u;
+          const float dcy = i <= t ? exp2f(gt - gam[i]) : 0.f;
+          pv[u] = dcy * gq[u];
+          av[u] = i < t ? bt * dcy * gk[u] : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) av[u] = pv[u] = 0.f;
       }
-      As[t * LDF + i] = a;
-      Ps[t * LDB + i] = __float2bfloat16_rn(p);
-      if ((i >> 4) > (t >> 4)) Tms[t * LDF + i] = 0.f;
+      *reinterpret_cast<float4*>(As + t * LDF + c8) = make_float4(av[0], av[1], av[2], av[3]);
+      *reinterpret_cast<float4*>(As + t * LDF + c8 + 4) = make_float4(av[4], av[5], av[6], av[7]);
+      *reinterpret_cast<uint4*>(Ps + t * LDB + c8) =
+          make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
+                     pack_bf16(pv[6], pv[7]));
+    }
+    if (gi == 0) {  // the blocks of Tm above the diagonal stay zero for every value head
+      for (int e = tid; e < kChunk * 16; e += kPrepThreads) {
+        const int t = e >> 4, c4 = (e & 15) * 4;
+        if ((c4 >> 4) > (t >> 4)) *reinterpret_cast<float4*>(Tms + t * LDF + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     __syncthreads();
 
     // ---- Tm: the four 16 x 16 diagonal blocks by forward substitution --------
+    // Column j of a block: x_j = 1, then for i = j, j+1, ...: x_{i+1} = -acc_{i+1}
+    // after every later acc_t has absorbed A[t][i] x_i (right-looking order, so
+    // the dependent chain is one FMA per row).
     if (tid < 64) {
       const int blk = tid >> 4, j = tid & 15;
       const float* Ab = As + 16 * blk * LDF + 16 * blk;
-      float x[16];
+      float x[16], accv[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
+      for (int i = 0; i < 16; ++i) { x[i] = (i == j) ? 1.f : 0.f; accv[i] = 0.f; }
 #pragma unroll
-      for (int t = 1; t < 16; ++t) {
-        float s = 0.f;
+      for (int i = 0; i < 15; ++i) {
+        if (i > j) x[i] = -accv[i];
 #pragma unroll
-        for (int i = 0; i < t; ++i) s = fmaf(Ab[t * LDF + i], x[i], s);
-        if (t > j) x[t] = -s;
+        for (int t = i + 1; t < 16; ++t) accv[t] = fmaf(Ab[t * LDF + i], x[i], accv[t]);
       }
+      if (15 > j) x[15] = -accv[15];
       float* Tb = Tms + 16 * blk * LDF + 16 * blk;
 #pragma unroll
       for (int t = 0; t < 16; ++t) Tb[t * LDF + j] = x[t];
@@ -367,17 +443,46 @@ gdn_chunk_table_kernel(const int32_t* __restrict__ cu, int B, int T, int32_t* __
 }
 
 // ---- launchers -----------------------------------------------------------------
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 prep_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+}  // namespace
+
 template <int DK>
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const float* beta,
-                        const int32_t* cu, const int32_t* chunk_off, void* ws, int B, int T,
+                        const int32_t* cu, const int32_t* chunk_off, void* ws, int* err, int B, int T,
                         int Hk, int Hv, int nslots, int nc_dense, cudaStream_t st) {
   using L = PrepSmem<DK>;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = prep_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
+  const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)Hk, (cuuint64_t)(ttot > 0 ? ttot : 1)};
+  const cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)Hk * DK * 2};
+  const cuuint32_t box[3] = {64, 1, 64}, es[3] = {1, 1, 1};
+  CUtensorMap mk, mq;
+  if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(gdn_prep_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::bytes);
   if (e != cudaSuccess) return e;
   dim3 grid(nslots, Hk);
-  gdn_prep_kernel<DK><<<grid, kPrepThreads, L::bytes, st>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g, beta, cu, chunk_off,
-      static_cast<__nv_bfloat16*>(ws), B, T, Hk, Hv, nc_dense);
+  gdn_prep_kernel<DK><<<grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
+                                                           static_cast<__nv_bfloat16*>(ws), err, B, T, Hk, Hv,
+                                                           nc_dense);
   return cudaGetLastError();
 }
 
@@ -386,11 +491,11 @@ cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_o
   return cudaGetLastError();
 }
 
-template cudaError_t launch_prep<32>(const void*, const void*, const float*, const float*, const int32_t*,
-                                     const int32_t*, void*, int, int, int, int, int, int, cudaStream_t);
-template cudaError_t launch_prep<64>(const void*, const void*, const float*, const float*, const int32_t*,
-                                     const int32_t*, void*, int, int, int, int, int, int, cudaStream_t);
-template cudaError_t launch_prep<128>(const void*, const void*, const float*, const float*, const int32_t*,
-                                      const int32_t*, void*, int, int, int, int, int, int, cudaStream_t);
+#define GDN_INST_PREP(DK)                                                                                  \
+  template cudaError_t launch_prep<DK>(const void*, const void*, const float*, const float*, const int32_t*, \
+                                       const int32_t*, void*, int*, int, int, int, int, int, int, cudaStream_t);
+GDN_INST_PREP(32)
+GDN_INST_PREP(64)
+GDN_INST_PREP(128)
 
 }  // namespace gdn
