@@ -82,7 +82,8 @@ struct PrepSmem {
   static constexpr int offTb = offP + kChunk * LDB * 2;
   static constexpr int offW = offTb + kChunk * LDB * 2;
   static constexpr int offGam = offW + 32 * LDW * 4;
-  static constexpr int offBar = offGam + 2 * kChunk * 4;
+  static constexpr int offGB = offGam + 2 * kChunk * 4;  // [2 buffers][g 64 | beta 64] fp32
+  static constexpr int offBar = offGB + 2 * 2 * kChunk * 4;
   static constexpr int bytes = offBar + 16 + 1024;  // + slack for 1024-byte alignment
 };
 
@@ -107,6 +108,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   float* gam = reinterpret_cast<float*>(smem + L::offGam);
   float* bet = gam + kChunk;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::offBar);
+  float* gbuf = reinterpret_cast<float*>(smem + L::offGB);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = blockIdx.x, hk = blockIdx.y;
@@ -130,6 +132,19 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const SeqChunk sq = seq_bounds(cu, b, T);
   const long long t0 = sq.bos + (long long)c * kChunk;
   const int n = min(kChunk, sq.len - c * kChunk);
+
+  // g and beta of one value head into buffer `buf` (zeros past the chunk's tokens)
+  const int G = Hv / Hk;
+  auto prefetch_gb = [&](int gi, int buf) {
+    if (tid < kChunk) {
+      const bool ok = tid < n;
+      const size_t off = ok ? (size_t)(t0 + tid) * Hv + hk * G + gi : 0;
+      cp_async4(gbuf + buf * 2 * kChunk + tid, g + off, ok);
+      cp_async4(gbuf + buf * 2 * kChunk + kChunk + tid, beta + off, ok);
+    }
+    cp_async_commit();
+  };
+  prefetch_gb(0, 0);
 
   // ---- load the K and Q tiles by TMA (tokens past the end of the tensor are zero)
   constexpr int kKBlocks = DK > 64 ? 2 : 1;
@@ -221,14 +236,17 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
   }
 
-  const int G = Hv / Hk;
   for (int gi = 0; gi < G; ++gi) {
     const int h = hk * G + gi;
+    // this head's g / beta arrived by cp.async; start fetching the next head's
+    cp_async_wait<0>();
+    __syncthreads();
+    if (gi + 1 < G) prefetch_gb(gi + 1, (gi + 1) & 1);
     // ---- gamma = inclusive cumsum of g in the chunk -------------------------
     if (warp == 0) {
-      float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-      if (lane < n) { g0 = g[(t0 + lane) * Hv + h]; b0 = beta[(t0 + lane) * Hv + h]; }
-      if (lane + 32 < n) { g1 = g[(t0 + lane + 32) * Hv + h]; b1 = beta[(t0 + lane + 32) * Hv + h]; }
+      const float* gb = gbuf + (gi & 1) * 2 * kChunk;
+      float g0 = gb[lane], g1 = gb[lane + 32];
+      const float b0 = gb[kChunk + lane], b1 = gb[kChunk + lane + 32];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float u0 = __shfl_up_sync(0xffffffffu, g0, o);
