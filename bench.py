@@ -220,6 +220,23 @@ def slice_tokens(inp, n):
     return s
 
 
+def whole_job_rate(local_ms, units_per_rank, world, device=None):
+    """Max-over-ranks step time (ms) and the whole-job rate: every rank's units over that time.
+
+    Each rank runs an independent replica, so per-rank work is fixed as ranks are added
+    (weak scaling) and there is no exchange step; the only collective is this MAX.
+    """
+    t_max = float(local_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([t_max], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    return world * units_per_rank / (t_max * 1e-3), t_max
+
+
 def run_gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -285,11 +302,7 @@ def run_gpu_arm(args):
     chain_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
     ms = statistics.mean(step_ms)
-    t_max = ms
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    rate, t_max = whole_job_rate(ms, Tt, world, dev)
 
     peaks = read_peaks()
     alg = algorithmic(inp)
@@ -312,12 +325,7 @@ def run_gpu_arm(args):
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(inp, gdn, torch, stream, max(3, min(args.e2e_steps, K)))
-        if world > 1:
-            tt = torch.tensor([e2e.pop("_ms")], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e["value"] = world * Tt / (float(tt.item()) * 1e-3)
-        else:
-            e2e["value"] = Tt / (e2e.pop("_ms") * 1e-3)
+        e2e["value"], _ = whole_job_rate(e2e.pop("_ms"), Tt, world, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -325,7 +333,7 @@ def run_gpu_arm(args):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": world * Tt / (t_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "B": B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv,
