@@ -20,6 +20,9 @@ template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
                             const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
                             int, long long, cudaStream_t);
+template <int DK>
+cudaError_t launch_decode(const void*, const void*, const void*, const float*, const float*, float*, void*, int,
+                          int, int, int, cudaStream_t);
 }  // namespace gdn
 
 namespace {
@@ -139,7 +142,7 @@ const char* gdn_strerror(int status) {
     case GDN_ERR_ALIGN: return "pointer not 16-byte aligned";
     case GDN_ERR_ALLOC: return "device workspace allocation failed";
     case GDN_ERR_LAUNCH: return "CUDA launch or runtime call failed";
-    case GDN_ERR_SCRATCH: return "problem too large for the fixed scratch of gdn_prefill_static";
+    case GDN_ERR_SCRATCH: return "problem needs more scratch than the fixed or caller-given workspace";
     default: return "unknown status";
   }
 }
@@ -186,6 +189,50 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
   }
   return launch_all(q, k, v, g, beta, cu_seqlens, init_state, out, final_state, B, T, Hk, Hv, dk, dv,
                     static_cast<cudaStream_t>(stream), ws);
+}
+
+int gdn_prefill_ws(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                   const int32_t* cu_seqlens, const float* init_state, void* out, float* final_state, int B,
+                   int T, int Hk, int Hv, int dk, int dv, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  t_last_cuda_error = 0;
+  int rc = check_sizes(B, T, Hk, Hv, dk, dv);
+  if (rc != GDN_OK) return rc;
+  if (B == 0) return GDN_OK;
+  const long long ntok = cu_seqlens != nullptr ? (long long)T : (long long)B * T;
+  if (ntok > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_ARG;
+  if (ntok > 0x7fffffffLL) return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, cu_seqlens, init_state, out, final_state};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return GDN_ERR_ALIGN;
+  if (ntok == 0 && final_state == nullptr) return GDN_OK;
+  if (workspace == nullptr) return GDN_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGN;
+  if (workspace_bytes < ws_bytes_for(B, T, Hv, cu_seqlens != nullptr)) return GDN_ERR_SCRATCH;
+  return launch_all(q, k, v, g, beta, cu_seqlens, init_state, out, final_state, B, T, Hk, Hv, dk, dv,
+                    static_cast<cudaStream_t>(stream), workspace);
+}
+
+int gdn_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, float* state,
+               void* out, int B, int Hk, int Hv, int dk, int dv, void* stream) {
+  t_last_cuda_error = 0;
+  int rc = check_sizes(B, 1, Hk, Hv, dk, dv);
+  if (rc != GDN_OK) return rc;
+  if (B == 0) return GDN_OK;
+  if ((long long)B * Hv > 0x7fffffffLL) return GDN_ERR_ARG;
+  if (!q || !k || !v || !g || !beta || !state || !out) return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, state, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return GDN_ERR_ALIGN;
+  cudaError_t e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (dk) {
+    case 32: e = gdn::launch_decode<32>(q, k, v, g, beta, state, out, B, Hk, Hv, dv, st); break;
+    case 64: e = gdn::launch_decode<64>(q, k, v, g, beta, state, out, B, Hk, Hv, dv, st); break;
+    default: e = gdn::launch_decode<128>(q, k, v, g, beta, state, out, B, Hk, Hv, dv, st); break;
+  }
+  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  return GDN_OK;
 }
 
 int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g, const float* beta,

@@ -457,8 +457,7 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
     const cuuint32_t box[2] = {64, 128};
     if (!make_map(&mw, ws, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(gdn_chain_tc_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
+  cudaError_t e = set_smem_limit_once<gdn_chain_tc_kernel<DK>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)B * (DV / kDVT), Hv);
   gdn_chain_tc_kernel<DK><<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, init,

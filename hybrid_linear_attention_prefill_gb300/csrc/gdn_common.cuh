@@ -101,4 +101,20 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// Raise a kernel's dynamic shared-memory limit once per device (a benign race if two
+// host threads do it at once).  Doing it once keeps later calls free of runtime
+// configuration calls, e.g. while a stream is being captured into a CUDA graph.
+// One flag set per kernel: the kernel itself is the template argument.
+template <auto kernel>
+inline cudaError_t set_smem_limit_once(int bytes) {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
 }  // namespace gdn

@@ -495,7 +495,7 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(gdn_prep_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::bytes);
+  cudaError_t e = set_smem_limit_once<gdn_prep_kernel<DK>>(L::bytes);
   if (e != cudaSuccess) return e;
   dim3 grid(nslots, Hk);
   gdn_prep_kernel<DK><<<grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,

@@ -27,8 +27,8 @@ GDN_ERR_SCRATCH = -5
 GDN_STATIC_SCRATCH_BYTES = 64 << 20
 
 EXPORTED = ("gdn_abi_version", "gdn_strerror", "gdn_last_cuda_error", "gdn_prefill",
-            "gdn_prefill_host", "gdn_prefill_static", "gdn_set_phase_events",
-            "gdn_workspace_bytes", "gdn_release_workspace")
+            "gdn_prefill_host", "gdn_prefill_static", "gdn_prefill_ws", "gdn_decode",
+            "gdn_set_phase_events", "gdn_workspace_bytes", "gdn_release_workspace")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +67,10 @@ def load(build_if_missing: bool = False):
         lib.gdn_prefill_host.restype = i
         lib.gdn_prefill_static.argtypes = sig
         lib.gdn_prefill_static.restype = i
+        lib.gdn_prefill_ws.argtypes = sig[:-1] + [vp, ctypes.c_size_t, vp]
+        lib.gdn_prefill_ws.restype = i
+        lib.gdn_decode.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]
+        lib.gdn_decode.restype = i
         lib.gdn_abi_version.argtypes = []
         lib.gdn_abi_version.restype = i
         lib.gdn_strerror.argtypes = [i]
@@ -157,6 +161,21 @@ def gdn_prefill_static(q, k, v, g, beta, cu_seqlens, init_state, out, final_stat
     return load().gdn_prefill_static(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
                                      _ptr(init_state), _ptr(out), _ptr(final_state),
                                      int(B), int(T), int(Hk), int(Hv), int(dk), int(dv), _stream(stream))
+
+
+def gdn_prefill_ws(q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
+                   B, T, Hk, Hv, dk, dv, workspace, workspace_bytes, stream=None) -> int:
+    """Call the caller-workspace entry point (no allocation, no host sync); returns the status."""
+    return load().gdn_prefill_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                 _ptr(init_state), _ptr(out), _ptr(final_state),
+                                 int(B), int(T), int(Hk), int(Hv), int(dk), int(dv),
+                                 _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def gdn_decode(q, k, v, g, beta, state, out, B, Hk, Hv, dk, dv, stream=None) -> int:
+    """One token per sequence, state updated in place; returns the status."""
+    return load().gdn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
+                             int(B), int(Hk), int(Hv), int(dk), int(dv), _stream(stream))
 
 
 def check(status: int) -> None:

@@ -39,7 +39,7 @@ extern "C" {
 #define GDN_ERR_ALIGN (-2)  /* a pointer is not 16-byte aligned */
 #define GDN_ERR_ALLOC (-3)  /* the library's device workspace could not be grown */
 #define GDN_ERR_LAUNCH (-4) /* a CUDA call or kernel launch failed (see gdn_last_cuda_error) */
-#define GDN_ERR_SCRATCH (-5) /* gdn_prefill_static: the problem needs more than its fixed scratch */
+#define GDN_ERR_SCRATCH (-5) /* the problem needs more scratch than the fixed or caller-given workspace */
 
 /* Size of the fixed device scratch array behind gdn_prefill_static (64 MiB per device). */
 #define GDN_STATIC_SCRATCH_BYTES (64u << 20)
@@ -104,6 +104,42 @@ int gdn_prefill_host(const void *q, const void *k, const void *v,
                      void *out, float *final_state,
                      int B, int T, int Hk, int Hv, int dk, int dv,
                      void *stream);
+
+/*
+ * gdn_prefill_ws -- gdn_prefill with a caller-owned workspace.
+ *
+ * Same arguments, layouts, alignment rules and status codes as gdn_prefill, plus
+ * `workspace` (device memory, 256-byte aligned, at least gdn_workspace_bytes(B, T,
+ * Hk, Hv, dk, dv, cu_seqlens != NULL) bytes, not shared with concurrent calls) and
+ * its size.  The call allocates nothing and never synchronises the host, so a
+ * caller can record it into a CUDA graph and replay it with new input values in
+ * the same buffers -- the calling convention behind the pages' per-prompt-length
+ * CUDA Graph replay ("Cua-S1 4B 0.2 native text worker", CUDA Graph paragraph).
+ * Returns GDN_ERR_SCRATCH when the workspace is too small, GDN_ERR_ALIGN when it
+ * is not 256-byte aligned.
+ */
+int gdn_prefill_ws(const void *q, const void *k, const void *v,
+                   const float *g, const float *beta,
+                   const int32_t *cu_seqlens, const float *init_state,
+                   void *out, float *final_state,
+                   int B, int T, int Hk, int Hv, int dk, int dv,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_decode -- one token per sequence on a carried state, the state updated in place.
+ *
+ *   q, k   bf16 [B, Hk, dk];  v bf16 [B, Hv, dv];  g, beta fp32 [B, Hv]
+ *   state  fp32 [B, Hv, dv, dk]  read as S_{t-1}, overwritten with S_t
+ *   out    bf16 [B, Hv, dv]      o_t = S_t q_t / sqrt(dk)
+ *
+ * The same recurrence as gdn_prefill applied to a single token, so a prefill of
+ * T tokens followed by gdn_decode of token T+1 matches a prefill of T+1 tokens.
+ * All pointers device memory, 16-byte aligned; out must not alias the inputs.
+ * Asynchronous on `stream`; allocates nothing.  Returns GDN_OK or an argument /
+ * alignment / launch error.
+ */
+int gdn_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
+               float *state, void *out, int B, int Hk, int Hv, int dk, int dv, void *stream);
 
 /*
  * gdn_set_phase_events -- timing hook for the NEXT gdn_prefill call on this host

@@ -86,3 +86,28 @@ def test_workspace_bytes(lib):
     assert gdn.gdn_workspace_bytes(1, 4096, 16, 32, 128, 128, 0) == 512 + 64 * 32 * per
     assert gdn.gdn_workspace_bytes(2, 100, 1, 1, 32, 32, 1) == 512 + (2 + 2) * per
     assert gdn.gdn_workspace_bytes(1, 10, 2, 3, 128, 128, 0) == 0
+
+
+def ws_call(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, cu_seqlens=None, init_state=None,
+             out=FAKE, final_state=None, B=1, T=64, Hk=1, Hv=1, dk=128, dv=128,
+             workspace=FAKE, workspace_bytes=1 << 30, stream=0)
+    a.update(kw)
+    return gdn.gdn_prefill_ws(**a)
+
+
+def test_caller_workspace_checks(lib):
+    assert ws_call(workspace=None) == gdn.GDN_ERR_ARG
+    assert ws_call(workspace=FAKE + 16) == gdn.GDN_ERR_ALIGN  # needs 256-byte alignment
+    need = gdn.gdn_workspace_bytes(1, 64, 1, 1, 128, 128, 0)
+    assert ws_call(workspace_bytes=need - 1) == gdn.GDN_ERR_SCRATCH
+    assert ws_call(B=0) == gdn.GDN_OK and ws_call(dk=48) == gdn.GDN_ERR_ARG
+
+
+def test_decode_argument_checks(lib):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state=FAKE, out=FAKE, B=2, Hk=1, Hv=2, dk=128,
+             dv=128, stream=0)
+    assert gdn.gdn_decode(**{**a, "state": None}) == gdn.GDN_ERR_ARG
+    assert gdn.gdn_decode(**{**a, "Hk": 2, "Hv": 3}) == gdn.GDN_ERR_ARG
+    assert gdn.gdn_decode(**{**a, "out": FAKE + 2}) == gdn.GDN_ERR_ALIGN
+    assert gdn.gdn_decode(**{**a, "B": 0}) == gdn.GDN_OK
