@@ -14,12 +14,12 @@
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, int*, int, int, int, int, int, int, cudaStream_t);
+                        void*, int*, int, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
                             const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
-                            int, long long, cudaStream_t);
+                            int, long long, int, cudaStream_t);
 template <int DK>
 cudaError_t launch_decode(const void*, const void*, const void*, const float*, const float*, float*, void*, int,
                           int, int, int, cudaStream_t);
@@ -94,7 +94,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int launch_all(const void* q, const void* k, const void* v, const float* g, const float* beta,
                const int32_t* cu, const float* init, void* out, float* fin, int B, int T, int Hk, int Hv,
-               int dk, int dv, cudaStream_t st, void* ws) {
+               int dk, int dv, cudaStream_t st, void* ws, int norm_qk = 0) {
   const int packed = cu != nullptr;
   int* err = static_cast<int*>(ws);
   int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + 256);
@@ -112,17 +112,17 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   if (nslots > 0) {
     if (nslots > 0x7fffffffLL) return GDN_ERR_ARG;
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, st); break;
     }
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
   if (ev[1] != nullptr && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, st); break;
   }
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
@@ -233,6 +233,37 @@ int gdn_decode(const void* q, const void* k, const void* v, const float* g, cons
   }
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   return GDN_OK;
+}
+
+int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                   const int32_t* cu_seqlens, const float* init_state, void* out, float* final_state, int B,
+                   int T, int Hk, int Hv, int dk, int dv, unsigned flags, void* stream) {
+  t_last_cuda_error = 0;
+  if ((flags & ~(unsigned)GDN_FLAG_L2NORM_QK) != 0) return GDN_ERR_ARG;
+  int rc = check_sizes(B, T, Hk, Hv, dk, dv);
+  if (rc != GDN_OK) return rc;
+  if (B == 0) return GDN_OK;
+  const long long ntok = cu_seqlens != nullptr ? (long long)T : (long long)B * T;
+  if (ntok > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_ARG;
+  if (ntok > 0x7fffffffLL) return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, cu_seqlens, init_state, out, final_state};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return GDN_ERR_ALIGN;
+  if (ntok == 0 && final_state == nullptr) return GDN_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_ARG;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevBuffers& d = g_dev[dev];
+    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hv, cu_seqlens != nullptr));
+    if (rc != GDN_OK) return rc;
+    ws = d.ws;
+  }
+  return launch_all(q, k, v, g, beta, cu_seqlens, init_state, out, final_state, B, T, Hk, Hv, dk, dv,
+                    static_cast<cudaStream_t>(stream), ws, (flags & GDN_FLAG_L2NORM_QK) ? 1 : 0);
 }
 
 int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g, const float* beta,

@@ -128,7 +128,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu,
                     const int32_t* __restrict__ chunk_off, const float* init, __nv_bfloat16* __restrict__ out,
                     float* fin, int* __restrict__ err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
-                    long long nslots) {
+                    long long nslots, int norm_qk) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
@@ -309,6 +309,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const float d_t = expf(glast - gam);
     const float eC = expf(glast);
     const float b_t = bs[tok];
+    // with in-kernel q/k normalisation, this token's inverse norm (k rows for the
+    // R / dU epilogues, q rows for the outputs); computed while phase 1 runs
+    const float rn = norm_qk ? tc::inv_norm(tc::row_sumsq_sw128<DK>(st + kOffKQ, tok + (q4 < 2 ? 0 : 64))) : 1.f;
 
     // ---- phase-1 epilogue: R = beta V - beta e X (rows 0..63), keep Y (rows 64..127)
     if (!tc::mbar_wait(&bars[0], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
@@ -317,7 +320,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     sum_parts<kP1>(tq, cg, acc);
     if (q4 < 2) {
       const unsigned char* vrow = st + kOffV;
-      const float be = b_t * e_t;
+      const float be = b_t * e_t * rn;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const uint4 raw = *reinterpret_cast<const uint4*>(vrow + tc::sw64(tok, 2 * cg + half));
@@ -334,7 +337,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       tc::fence_proxy_async();  // R is read by the tensor core next
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = acc[i];
+      for (int i = 0; i < 16; ++i) y[i] = acc[i] * rn;
     }
     tc::fence_before();
     __syncthreads();  // R written
@@ -346,8 +349,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     sum_parts<kParts23>(tq, cg, acc);
     uint32_t o8[8];
     if (q4 < 2) {
+      const float dr = d_t * rn;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] *= d_t;
+      for (int i = 0; i < 16; ++i) acc[i] *= dr;
       store_split16(sm + kOffU, tok, cg, acc);
       tc::fence_proxy_async();  // dU is read by the tensor core next
     } else {
@@ -432,7 +436,7 @@ template <int DK>
 cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const int32_t* cu, const int32_t* chunk_off, const void* ws, const float* init,
                             void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
-                            long long nslots, cudaStream_t st) {
+                            long long nslots, int norm_qk, cudaStream_t st) {
   const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
   const cuuint64_t tt = (cuuint64_t)(ttot > 0 ? ttot : 1);
   CUtensorMap mk, mq, mv, mw;
@@ -462,14 +466,15 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
   dim3 grid((unsigned)B * (DV / kDVT), Hv);
   gdn_chain_tc_kernel<DK><<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, init,
                                                                static_cast<__nv_bfloat16*>(out), fin, err, B, T,
-                                                               Hk, Hv, DV, nc_dense, nslots);
+                                                               Hk, Hv, DV, nc_dense, nslots, norm_qk);
   return cudaGetLastError();
 }
 
 #define GDN_INST_CHAIN_TC(DK)                                                                                \
   template cudaError_t launch_chain_tc<DK>(const void*, const void*, const void*, const float*, const float*, \
                                            const int32_t*, const int32_t*, const void*, const float*, void*,  \
-                                           float*, int*, int, int, int, int, int, int, long long, cudaStream_t);
+                                           float*, int*, int, int, int, int, int, int, long long, int,        \
+                                           cudaStream_t);
 GDN_INST_CHAIN_TC(32)
 GDN_INST_CHAIN_TC(64)
 GDN_INST_CHAIN_TC(128)

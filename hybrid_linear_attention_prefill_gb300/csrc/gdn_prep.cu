@@ -82,7 +82,8 @@ struct PrepSmem {
   static constexpr int offTb = offP + kChunk * LDB * 2;
   static constexpr int offW = offTb + kChunk * LDB * 2;
   static constexpr int offGam = offW + 32 * LDW * 4;
-  static constexpr int offGB = offGam + 2 * kChunk * 4;  // [2 buffers][g 64 | beta 64] fp32
+  static constexpr int offRN = offGam + 2 * kChunk * 4;  // inverse norms of k rows, then q rows
+  static constexpr int offGB = offRN + 2 * kChunk * 4;   // [2 buffers][g 64 | beta 64] fp32
   static constexpr int offBar = offGB + 2 * 2 * kChunk * 4;
   static constexpr int bytes = offBar + 16 + 1024;  // + slack for 1024-byte alignment
 };
@@ -93,7 +94,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 const float* __restrict__ g, const float* __restrict__ beta,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_off,
                 __nv_bfloat16* __restrict__ ws, int* __restrict__ err, int B, int T, int Hk, int Hv,
-                int nc_dense) {
+                int nc_dense, int norm_qk) {
   using L = PrepSmem<DK>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -109,6 +110,8 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   float* bet = gam + kChunk;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::offBar);
   float* gbuf = reinterpret_cast<float*>(smem + L::offGB);
+  float* rnk = reinterpret_cast<float*>(smem + L::offRN);  // 1/||k_t|| (1 without normalisation)
+  float* rnq = rnk + kChunk;                                // 1/||q_t||
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = blockIdx.x, hk = blockIdx.y;
@@ -236,6 +239,13 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
   }
 
+  // inverse norms of the k and q rows, read before the K/Q tiles are overwritten
+  if (tid < 2 * kChunk) {
+    const float r = norm_qk ? tc::inv_norm(tc::row_sumsq_sw128<DK>(KQ, (tid & 63) + 64 * (tid >> 6))) : 1.f;
+    rnk[tid] = r;  // tid 0..63: k rows, 64..127: q rows (rnq = rnk + 64)
+  }
+  __syncthreads();
+
   for (int gi = 0; gi < G; ++gi) {
     const int h = hk * G + gi;
     // this head's g / beta arrived by cp.async; start fetching the next head's
@@ -268,14 +278,14 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       const int t = e >> 3, c8 = (e & 7) * 8;
       float av[8], pv[8];
       if (c8 <= t) {
-        const float gt = gam[t], bt = bet[t];
+        const float gt = gam[t], bt = bet[t] * rnk[t], qt = rnq[t];
         const float* gk = Gs + t * LDF + c8;
         const float* gq = Gs + kChunk * LDF + t * LDF + c8;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int i = c8 + u;
-          const float dcy = i <= t ? exp2f(gt - gam[i]) : 0.f;
-          pv[u] = dcy * gq[u];
+          const float dcy = i <= t ? exp2f(gt - gam[i]) * rnk[i] : 0.f;
+          pv[u] = qt * dcy * gq[u];
           av[u] = i < t ? bt * dcy * gk[u] : 0.f;
         }
       } else {
@@ -479,7 +489,7 @@ PFN_cuTensorMapEncodeTiled_v12000 prep_map_encoder() {
 template <int DK>
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const float* beta,
                         const int32_t* cu, const int32_t* chunk_off, void* ws, int* err, int B, int T,
-                        int Hk, int Hv, int nslots, int nc_dense, cudaStream_t st) {
+                        int Hk, int Hv, int nslots, int nc_dense, int norm_qk, cudaStream_t st) {
   using L = PrepSmem<DK>;
   PFN_cuTensorMapEncodeTiled_v12000 enc = prep_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -500,7 +510,7 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   dim3 grid(nslots, Hk);
   gdn_prep_kernel<DK><<<grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
                                                            static_cast<__nv_bfloat16*>(ws), err, B, T, Hk, Hv,
-                                                           nc_dense);
+                                                           nc_dense, norm_qk);
   return cudaGetLastError();
 }
 
@@ -511,7 +521,7 @@ cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_o
 
 #define GDN_INST_PREP(DK)                                                                                  \
   template cudaError_t launch_prep<DK>(const void*, const void*, const float*, const float*, const int32_t*, \
-                                       const int32_t*, void*, int*, int, int, int, int, int, int, cudaStream_t);
+                                       const int32_t*, void*, int*, int, int, int, int, int, int, int, cudaStream_t);
 GDN_INST_PREP(32)
 GDN_INST_PREP(64)
 GDN_INST_PREP(128)

@@ -192,5 +192,28 @@ __device__ __forceinline__ uint32_t sw64(uint32_t row, uint32_t chunk) {
   return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
 }
 
+// Sum of squares of row `row` of a bf16 tile stored as [dk/64 blocks of 16 KB]
+// [rows][128 B] with the 128-byte swizzle, over its first DK elements (fixed order,
+// so every kernel gets the same value for the same row).
+template <int DK>
+__device__ __forceinline__ float row_sumsq_sw128(const unsigned char* tile, int row) {
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < DK / 8; ++c) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(tile + (c >> 3) * 16384 + sw128(row, c & 7));
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[p]));
+      s = fmaf(f.x, f.x, s);
+      s = fmaf(f.y, f.y, s);
+    }
+  }
+  return s;
+}
+
+// 1 / max(||x||, 1e-6): the inverse L2 norm used when q and k are normalised in-kernel.
+__device__ __forceinline__ float inv_norm(float sumsq) { return rsqrtf(fmaxf(sumsq, 1e-12f)); }
+
 }  // namespace tc
 }  // namespace gdn

@@ -25,9 +25,10 @@ GDN_ERR_ALLOC = -3
 GDN_ERR_LAUNCH = -4
 GDN_ERR_SCRATCH = -5
 GDN_STATIC_SCRATCH_BYTES = 64 << 20
+GDN_FLAG_L2NORM_QK = 1
 
 EXPORTED = ("gdn_abi_version", "gdn_strerror", "gdn_last_cuda_error", "gdn_prefill",
-            "gdn_prefill_host", "gdn_prefill_static", "gdn_prefill_ws", "gdn_decode",
+            "gdn_prefill_host", "gdn_prefill_static", "gdn_prefill_ws", "gdn_prefill_ex", "gdn_decode",
             "gdn_set_phase_events", "gdn_workspace_bytes", "gdn_release_workspace")
 
 _lock = threading.Lock()
@@ -69,6 +70,8 @@ def load(build_if_missing: bool = False):
         lib.gdn_prefill_static.restype = i
         lib.gdn_prefill_ws.argtypes = sig[:-1] + [vp, ctypes.c_size_t, vp]
         lib.gdn_prefill_ws.restype = i
+        lib.gdn_prefill_ex.argtypes = sig[:-1] + [ctypes.c_uint, vp]
+        lib.gdn_prefill_ex.restype = i
         lib.gdn_decode.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]
         lib.gdn_decode.restype = i
         lib.gdn_abi_version.argtypes = []
@@ -170,6 +173,15 @@ def gdn_prefill_ws(q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
                                  _ptr(init_state), _ptr(out), _ptr(final_state),
                                  int(B), int(T), int(Hk), int(Hv), int(dk), int(dv),
                                  _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def gdn_prefill_ex(q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
+                   B, T, Hk, Hv, dk, dv, flags, stream=None) -> int:
+    """gdn_prefill with option flags (GDN_FLAG_L2NORM_QK); returns the status."""
+    return load().gdn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                 _ptr(init_state), _ptr(out), _ptr(final_state),
+                                 int(B), int(T), int(Hk), int(Hv), int(dk), int(dv), int(flags),
+                                 _stream(stream))
 
 
 def gdn_decode(q, k, v, g, beta, state, out, B, Hk, Hv, dk, dv, stream=None) -> int:

@@ -127,9 +127,10 @@ def make_gdn_inputs(
     seed: int = 0,
     g_scale: float = 1.0,
     init_std: Optional[float] = None,
+    normalize_qk: bool = True,
     name: str = "",
 ) -> GdnInputs:
-    """Draw one seeded problem.
+    """Draw one seeded problem (``normalize_qk=False`` leaves q and k un-normalised).
 
     Dense: ``B`` sequences of ``T`` tokens (cu_seqlens None unless ``packed``).
     Packed: ``lengths`` is a list of sequence lengths, or ``("uniform", n, lo, hi)``
@@ -153,8 +154,10 @@ def make_gdn_inputs(
             cu = np.arange(B + 1, dtype=np.int32) * T
             T = Ttot
     f32 = np.float32
-    q = _l2_normalise(rng.standard_normal((Ttot, Hk, dk), dtype=f32))
-    k = _l2_normalise(rng.standard_normal((Ttot, Hk, dk), dtype=f32))
+    q = rng.standard_normal((Ttot, Hk, dk), dtype=f32)
+    k = rng.standard_normal((Ttot, Hk, dk), dtype=f32)
+    if normalize_qk:  # the caller's per-token normalisation (else raw projections)
+        q, k = _l2_normalise(q), _l2_normalise(k)
     v = rng.standard_normal((Ttot, Hv, dv), dtype=f32)
     g = (-_softplus(rng.standard_normal((Ttot, Hv), dtype=f32)) * f32(g_scale)).astype(f32)
     beta = _sigmoid(rng.standard_normal((Ttot, Hv), dtype=f32))

@@ -41,6 +41,9 @@ extern "C" {
 #define GDN_ERR_LAUNCH (-4) /* a CUDA call or kernel launch failed (see gdn_last_cuda_error) */
 #define GDN_ERR_SCRATCH (-5) /* the problem needs more scratch than the fixed or caller-given workspace */
 
+/* Flags of gdn_prefill_ex. */
+#define GDN_FLAG_L2NORM_QK 1u /* normalise q and k per token inside the kernels: x / max(||x||, 1e-6) */
+
 /* Size of the fixed device scratch array behind gdn_prefill_static (64 MiB per device). */
 #define GDN_STATIC_SCRATCH_BYTES (64u << 20)
 
@@ -104,6 +107,24 @@ int gdn_prefill_host(const void *q, const void *k, const void *v,
                      void *out, float *final_state,
                      int B, int T, int Hk, int Hv, int dk, int dv,
                      void *stream);
+
+/*
+ * gdn_prefill_ex -- gdn_prefill with option flags.
+ *
+ * GDN_FLAG_L2NORM_QK: q and k are taken as they come out of the projections and
+ * L2-normalised per token inside the kernels (the pages run this normalisation
+ * as a separate fused "norm ... QK" operation before the prefill; "Open-Jev-27B-v1.1
+ * native text worker", "Validation and optimization scope").  The norms are summed
+ * in fp32 from the bf16 inputs and applied as row scalings of the fp32 products, so
+ * no normalised copy of q or k is written.  Unknown flag bits are GDN_ERR_ARG.
+ * Everything else as gdn_prefill.
+ */
+int gdn_prefill_ex(const void *q, const void *k, const void *v,
+                   const float *g, const float *beta,
+                   const int32_t *cu_seqlens, const float *init_state,
+                   void *out, float *final_state,
+                   int B, int T, int Hk, int Hv, int dk, int dv,
+                   unsigned flags, void *stream);
 
 /*
  * gdn_prefill_ws -- gdn_prefill with a caller-owned workspace.

@@ -111,3 +111,10 @@ def test_decode_argument_checks(lib):
     assert gdn.gdn_decode(**{**a, "Hk": 2, "Hv": 3}) == gdn.GDN_ERR_ARG
     assert gdn.gdn_decode(**{**a, "out": FAKE + 2}) == gdn.GDN_ERR_ALIGN
     assert gdn.gdn_decode(**{**a, "B": 0}) == gdn.GDN_OK
+
+
+def test_prefill_ex_rejects_unknown_flags(lib):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, cu_seqlens=None, init_state=None,
+             out=FAKE, final_state=None, B=1, T=64, Hk=1, Hv=1, dk=128, dv=128, stream=0)
+    assert gdn.gdn_prefill_ex(**a, flags=2) == gdn.GDN_ERR_ARG
+    assert gdn.gdn_prefill_ex(**{**a, "B": 0}, flags=gdn.GDN_FLAG_L2NORM_QK) == gdn.GDN_OK
