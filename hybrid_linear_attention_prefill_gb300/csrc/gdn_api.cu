@@ -20,6 +20,7 @@ template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
                             const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
                             int, long long, int, cudaStream_t);
+cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 template <int DK>
 cudaError_t launch_decode(const void*, const void*, const void*, const float*, const float*, float*, void*, int,
                           int, int, int, cudaStream_t);
@@ -323,6 +324,44 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
   e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  return GDN_OK;
+}
+
+int gdn_device_status(int* status) {
+  t_last_cuda_error = 0;
+  if (status == nullptr) return GDN_ERR_ARG;
+  *status = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_ARG;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ws = g_dev[dev].ws;
+  }
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  if (ws == nullptr) return GDN_OK;
+  e = cudaMemcpy(status, ws, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  e = cudaMemset(ws, 0, sizeof(int));
+  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  return GDN_OK;
+}
+
+int gdn_selftest_wait_timeout(int max_polls, int* status) {
+  t_last_cuda_error = 0;
+  if (status == nullptr || max_polls < 1) return GDN_ERR_ARG;
+  int* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, sizeof(int));
+  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_ALLOC);
+  e = cudaMemset(d, 0, sizeof(int));
+  if (e == cudaSuccess) e = gdn::launch_wait_timeout_probe(max_polls, d, nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(status, d, sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFree(d);
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   return GDN_OK;
 }

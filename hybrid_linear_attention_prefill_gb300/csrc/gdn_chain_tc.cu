@@ -404,6 +404,23 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// The bounded-wait path of the kernels, run on purpose: an mbarrier that nothing
+// completes, waited on with the same helper and the same give-up handling.
+__global__ void gdn_wait_timeout_probe_kernel(int max_polls, int* __restrict__ status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (!tc::mbar_wait(&bar, 0, (uint32_t)max_polls)) atomicOr(status, 1);
+}
+
+cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st) {
+  gdn_wait_timeout_probe_kernel<<<1, 32, 0, st>>>(max_polls, status);
+  return cudaGetLastError();
+}
+
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {

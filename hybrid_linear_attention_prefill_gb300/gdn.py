@@ -26,10 +26,14 @@ GDN_ERR_LAUNCH = -4
 GDN_ERR_SCRATCH = -5
 GDN_STATIC_SCRATCH_BYTES = 64 << 20
 GDN_FLAG_L2NORM_QK = 1
+GDN_STATUS_MMA_TIMEOUT = 1
+GDN_STATUS_LOAD_TIMEOUT = 2
+GDN_STATUS_PREP_LOAD_TIMEOUT = 4
 
 EXPORTED = ("gdn_abi_version", "gdn_strerror", "gdn_last_cuda_error", "gdn_prefill",
             "gdn_prefill_host", "gdn_prefill_static", "gdn_prefill_ws", "gdn_prefill_ex", "gdn_decode",
-            "gdn_set_phase_events", "gdn_workspace_bytes", "gdn_release_workspace")
+            "gdn_set_phase_events", "gdn_workspace_bytes", "gdn_release_workspace",
+            "gdn_device_status", "gdn_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +88,10 @@ def load(build_if_missing: bool = False):
         lib.gdn_workspace_bytes.restype = ctypes.c_size_t
         lib.gdn_set_phase_events.argtypes = [vp, vp, vp]
         lib.gdn_set_phase_events.restype = None
+        lib.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        lib.gdn_device_status.restype = i
+        lib.gdn_selftest_wait_timeout.argtypes = [i, ctypes.POINTER(ctypes.c_int)]
+        lib.gdn_selftest_wait_timeout.restype = i
         lib.gdn_release_workspace.argtypes = []
         lib.gdn_release_workspace.restype = None
         _lib = lib
@@ -136,6 +144,20 @@ def gdn_set_phase_events(ev_begin, ev_mid, ev_end) -> None:
             return e
         return e.cuda_event
     load().gdn_set_phase_events(h(ev_begin), h(ev_mid), h(ev_end))
+
+
+def gdn_device_status():
+    """(status code, device status bits of the library workspace); clears the bits."""
+    st = ctypes.c_int(0)
+    rc = load().gdn_device_status(ctypes.byref(st))
+    return rc, st.value
+
+
+def gdn_selftest_wait_timeout(max_polls):
+    """(status code, recorded bits) of a bounded wait that is made to run out."""
+    st = ctypes.c_int(0)
+    rc = load().gdn_selftest_wait_timeout(int(max_polls), ctypes.byref(st))
+    return rc, st.value
 
 
 def gdn_release_workspace() -> None:

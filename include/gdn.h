@@ -199,6 +199,33 @@ int gdn_prefill_static(const void *q, const void *k, const void *v,
                        int B, int T, int Hk, int Hv, int dk, int dv,
                        void *stream);
 
+/*
+ * Device status bits.  Every wait inside the kernels (on an MMA completion or a
+ * TMA load) is bounded; a wait that runs out sets one of these bits in the first
+ * word of the workspace, lets its copies and MMAs in flight land (bounded again),
+ * frees its tensor memory and returns, so the context stays usable.  With
+ * gdn_prefill_ws the word is the first 4 bytes of the caller's workspace.
+ */
+#define GDN_STATUS_MMA_TIMEOUT 1       /* the state-carry kernel gave up waiting for an MMA phase */
+#define GDN_STATUS_LOAD_TIMEOUT 2      /* the state-carry kernel gave up waiting for a tile load */
+#define GDN_STATUS_PREP_LOAD_TIMEOUT 4 /* the preparation kernel gave up waiting for a tile load */
+
+/*
+ * gdn_device_status -- synchronise the current device, return the status bits
+ * accumulated in the library workspace since the last call (in *status) and
+ * clear them.  Returns GDN_OK or GDN_ERR_LAUNCH.
+ */
+int gdn_device_status(int *status);
+
+/*
+ * gdn_selftest_wait_timeout -- run the bounded-wait path on purpose: one CTA
+ * waits on an mbarrier that nothing completes, gives up after `max_polls` polls,
+ * and records GDN_STATUS_MMA_TIMEOUT, exactly as the kernels do.  *status gets
+ * the recorded bits (synchronous).  Used to test failure detection without a GPU
+ * fault.
+ */
+int gdn_selftest_wait_timeout(int max_polls, int *status);
+
 /* Bytes of device workspace gdn_prefill needs for these sizes (0 on bad arguments). */
 size_t gdn_workspace_bytes(int B, int T, int Hk, int Hv, int dk, int dv, int packed);
 
