@@ -266,9 +266,14 @@ def run_gpu_arm(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    flags = {"auto": None, "one": gdn.GDN_FLAG_ONE_LEVEL, "two": gdn.GDN_FLAG_TWO_LEVEL}[args.levels]
+
     def step():
-        return gdn.gdn_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], d["init"], out, fin,
-                               B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, stream)
+        if flags is None:
+            return gdn.gdn_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], d["init"], out, fin,
+                                   B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, stream)
+        return gdn.gdn_prefill_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], d["init"], out, fin,
+                                  B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, flags, stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -310,11 +315,15 @@ def run_gpu_arm(args):
     dom = max(kernels, key=kernels.get)
     dom_bytes = alg["chain"] if dom == "gdn_chain_kernel" else alg["prep"]
     achieved = dom_bytes / (kernels[dom] * 1e-3) / 1e9
-    trec = traffic_record(dom)
+    segs = gdn.gdn_scan_segments(B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, d["cu"] is not None,
+                                 0 if flags is None else flags)
+    trec = traffic_record(dom) if segs == 1 else None  # the ncu record is of the single-level launch
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
                 "traffic": None if trec is None else trec["dram_bytes_per_launch"],
                 "peak_source": peaks["source"]}
+    if segs > 1:
+        roofline["kernel"] = f"{dom} (two-level scan, {segs} segments: three launches)"
     t_hbm = alg["total"] / (peaks["hbm"] * 1e9)
     t_tc = alg["flops"] / (peaks["bf16"] * 1e12)
     path_roof = {"roofline_us": round(max(t_hbm, t_tc) * 1e6, 2), "bound": "hbm" if t_hbm >= t_tc else "tensor",
@@ -339,12 +348,14 @@ def run_gpu_arm(args):
             "config": {"workload": args.workload, "B": B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv,
                        "dk": inp.dk, "dv": inp.dv, "tokens": Tt,
                        "l2": "flushed between timed steps (256 MB write)",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}", "levels": args.levels},
             "roofline": roofline, "path_roofline": path_roof,
             "kernels_us": {k: round(v * 1e3, 2) for k, v in kernels.items()},
             "ms_per_step_min": min(step_ms), "wall_s": round(wall, 3),
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": K * (2 + (inp.cu_seqlens is not None)),
+            # prep + state carry (+ chunk table when packed); the two-level scan adds the
+            # segment set-up, its chunk table, a second pass-A carry, the combine and pass C
+            "gpu_launches": K * (2 + (inp.cu_seqlens is not None) if segs == 1 else 7),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -433,6 +444,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--levels", choices=["auto", "one", "two"], default="auto",
+                    help="chunk scan: the library's choice, single-level only, or two-level")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -6,6 +6,7 @@
 // follows the pages' native CUDA library ("Cua-S1 4B 0.2 native text worker",
 // CUDA Graph paragraph; "Open-Jev-27B-v1.1 native text worker", "Build and
 // serve" and "Prepare the checkpoint").
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/gdn.h"
@@ -21,6 +22,9 @@ cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*,
                             const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
                             int, long long, int, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
+cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int, int, int, int, int, int, int, cudaStream_t);
+cudaError_t launch_seg_combine(const float*, const float*, const float*, float*, int, int, int, int, int,
+                               cudaStream_t);
 template <int DK>
 cudaError_t launch_decode(const void*, const void*, const void*, const float*, const float*, float*, void*, int,
                           int, int, int, cudaStream_t);
@@ -35,6 +39,12 @@ struct DevBuffers {
   size_t ws_bytes = 0;
   void* stage = nullptr;  // device staging for gdn_prefill_host
   size_t stage_bytes = 0;
+  void* scan = nullptr;   // two-level scan buffers (its first bytes: an all-zero value tensor)
+  size_t scan_bytes = 0;
+  size_t scan_zeroed = 0;
+  cudaStream_t aux = nullptr;  // second stream for pass A's transition run
+  cudaEvent_t fork = nullptr, join = nullptr;
+  int sms = 0;
 };
 
 std::mutex g_mu;
@@ -93,9 +103,115 @@ int ensure(void*& ptr, size_t& have, size_t need) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---- two-level chunk scan (dense batches with few heads and many chunks) -----------
+// Number of segments P (1 = the single-level path).  Pass A runs B P Hv (dv + dk) / 32
+// state-carry CTAs at once, so P is what fits one wave on the device's SMs, at least
+// 3 (with 2 the two passes take as long as one unsegmented pass) and at most one
+// segment per 4 chunks.
+int choose_segments(int B, int T, int Hv, int dk, int dv, bool packed, unsigned flags, int sms) {
+  if (packed || (flags & GDN_FLAG_ONE_LEVEL) != 0 || B <= 0 || T <= 0) return 1;
+  const long long nc = (T + gdn::kChunk - 1) / gdn::kChunk;
+  const long long per_seg = std::max<long long>(1, (long long)B * Hv * (dv + dk) / 32);
+  const long long fit = sms / per_seg;
+  const int req = (int)((flags >> 8) & 0xffu);
+  if ((flags & GDN_FLAG_TWO_LEVEL) != 0) {
+    long long P = req >= 2 ? req : std::max<long long>(3, fit);
+    P = std::min(P, nc);
+    return P >= 2 ? (int)P : 1;
+  }
+  long long P = std::min<long long>(std::min<long long>(fit, nc / 4), 32);
+  return P >= 3 ? (int)P : 1;
+}
+
+struct ScanLayout {
+  size_t vzero, oscr, cu, off, a_init, i_init, n_fin, phi, c_init, f_fin, total;
+};
+
+ScanLayout scan_layout(int B, int T, int Hv, int dk, int dv, int P) {
+  ScanLayout L;
+  const size_t ntok = (size_t)B * T, bp = (size_t)B * P;
+  const size_t st = bp * Hv * dv * dk * 4, sp = bp * Hv * dk * dk * 4;
+  size_t o = 0;
+  auto take = [&](size_t n) { const size_t r = o; o += align_up(n, 256); return r; };
+  L.vzero = take(ntok * Hv * dk * 2);  // first, so the zeroed prefix only ever grows
+  L.oscr = take(ntok * Hv * dk * 2);
+  L.cu = take((bp + 1) * 4);
+  L.off = take((bp + 1) * 4);
+  L.a_init = take(st);
+  L.i_init = take(sp);
+  L.n_fin = take(st);
+  L.phi = take(sp);
+  L.c_init = take(st);
+  L.f_fin = take(st);
+  L.total = o;
+  return L;
+}
+
+struct ScanPlan {
+  int P = 1;
+  unsigned char* buf = nullptr;
+  cudaStream_t aux = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+// Segment count and (when P > 1) buffers, stream and events for the calling device.
+int prepare_scan(int dev, int B, int T, int Hv, int dk, int dv, bool packed, unsigned flags, cudaStream_t st,
+                 ScanPlan& plan) {
+  DevBuffers& d = g_dev[dev];
+  if (d.sms == 0) {
+    cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  }
+  plan.P = choose_segments(B, T, Hv, dk, dv, packed, flags, d.sms);
+  if (plan.P <= 1) return GDN_OK;
+  const ScanLayout L = scan_layout(B, T, Hv, dk, dv, plan.P);
+  void* before = d.scan;
+  int rc = ensure(d.scan, d.scan_bytes, L.total);
+  if (rc != GDN_OK) return rc;
+  if (d.scan != before) d.scan_zeroed = 0;  // a new allocation
+  if (L.oscr > d.scan_zeroed) {  // the zero value tensor of the transition run
+    cudaError_t e = cudaMemsetAsync(d.scan, 0, L.oscr, st);
+    if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  }
+  // this call writes its scratch outputs right after the zero tensor, so only that
+  // tensor is known to be zero afterwards
+  d.scan_zeroed = L.oscr;
+  if (d.aux == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&d.aux, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  }
+  plan.buf = static_cast<unsigned char*>(d.scan);
+  plan.aux = d.aux;
+  plan.fork = d.fork;
+  plan.join = d.join;
+  return GDN_OK;
+}
+
+template <int DK>
+cudaError_t chain(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* init, void* out,
+                  float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots,
+                  int norm_qk, cudaStream_t st) {
+  return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, DV,
+                                  nc_dense, nslots, norm_qk, st);
+}
+
+cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const float* g, const float* beta,
+                     const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* init, void* out,
+                     float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots,
+                     int norm_qk, cudaStream_t st) {
+  switch (dk) {
+    case 32: return chain<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
+    case 64: return chain<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
+    default: return chain<128>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
+  }
+}
+
 int launch_all(const void* q, const void* k, const void* v, const float* g, const float* beta,
                const int32_t* cu, const float* init, void* out, float* fin, int B, int T, int Hk, int Hv,
-               int dk, int dv, cudaStream_t st, void* ws, int norm_qk = 0) {
+               int dk, int dv, cudaStream_t st, void* ws, int norm_qk = 0, const ScanPlan* plan = nullptr) {
   const int packed = cu != nullptr;
   int* err = static_cast<int*>(ws);
   int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + 256);
@@ -120,6 +236,52 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
   if (ev[1] != nullptr && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  if (plan != nullptr && plan->P > 1 && !packed && nslots > 0) {
+    // ---- two-level scan over P segments per sequence (see gdn_scan.cu) ----------------
+    const int P = plan->P, BP = B * P;
+    const int cps = (nc_dense + P - 1) / P;  // chunks per segment
+    const ScanLayout L = scan_layout(B, T, Hv, dk, dv, P);
+    unsigned char* sb = plan->buf;
+    void* vzero = sb + L.vzero;
+    void* oscr = sb + L.oscr;
+    int32_t* cu_seg = reinterpret_cast<int32_t*>(sb + L.cu);
+    int32_t* off_seg = reinterpret_cast<int32_t*>(sb + L.off);
+    float* a_init = reinterpret_cast<float*>(sb + L.a_init);
+    float* i_init = reinterpret_cast<float*>(sb + L.i_init);
+    float* n_fin = reinterpret_cast<float*>(sb + L.n_fin);
+    float* phi = reinterpret_cast<float*>(sb + L.phi);
+    float* c_init = reinterpret_cast<float*>(sb + L.c_init);
+    float* f_fin = reinterpret_cast<float*>(sb + L.f_fin);
+    const int ttot = B * T;
+    if ((e = gdn::launch_seg_setup(init, a_init, i_init, cu_seg, B, T, P, cps, Hv, dv, dk, st)) != cudaSuccess ||
+        (e = gdn::launch_chunk_table(cu_seg, BP, ttot, off_seg, st)) != cudaSuccess ||
+        (e = cudaEventRecord(plan->fork, st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(plan->aux, plan->fork, 0)) != cudaSuccess)
+      return set_cuda_error(e, GDN_ERR_LAUNCH);
+    // pass A: transition matrices (v = 0 from the identity, dk rows) beside the zero-start runs
+    if ((e = chain_dk(dk, q, k, vzero, g, beta, cu_seg, off_seg, tiles, i_init, oscr, phi, err, BP, ttot, Hk,
+                      Hv, dk, nc_dense, nslots, norm_qk, plan->aux)) != cudaSuccess ||
+        (e = chain_dk(dk, q, k, v, g, beta, cu_seg, off_seg, tiles, a_init, out, n_fin, err, BP, ttot, Hk, Hv,
+                      dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess ||
+        (e = cudaEventRecord(plan->join, plan->aux)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, plan->join, 0)) != cudaSuccess)
+      return set_cuda_error(e, GDN_ERR_LAUNCH);
+    // segment start states, then pass C from them (outputs; the last segment's final state)
+    if ((e = gdn::launch_seg_combine(init, n_fin, phi, c_init, B, P, Hv, dv, dk, st)) != cudaSuccess ||
+        (e = chain_dk(dk, q, k, v, g, beta, cu_seg, off_seg, tiles, c_init, out, f_fin, err, BP, ttot, Hk, Hv,
+                      dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess)
+      return set_cuda_error(e, GDN_ERR_LAUNCH);
+    if (fin != nullptr) {
+      const size_t per = (size_t)Hv * dv * dk;
+      for (int b = 0; b < B; ++b) {
+        e = cudaMemcpyAsync(fin + (size_t)b * per, f_fin + ((size_t)b * P + P - 1) * per, per * sizeof(float),
+                            cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+      }
+    }
+    if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+    return GDN_OK;
+  }
   switch (dk) {
     case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, st); break;
     case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, st); break;
@@ -156,6 +318,19 @@ void gdn_set_phase_events(void* ev_begin, void* ev_mid, void* ev_end) {
   t_phase_ev[2] = static_cast<cudaEvent_t>(ev_end);
 }
 
+int gdn_scan_segments(int B, int T, int Hk, int Hv, int dk, int dv, int packed, unsigned flags) {
+  const unsigned known = GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u;
+  if (check_sizes(B, T, Hk, Hv, dk, dv) != GDN_OK || (flags & ~known) != 0) return 0;
+  if ((flags & GDN_FLAG_TWO_LEVEL) && (flags & GDN_FLAG_ONE_LEVEL)) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return choose_segments(B, T, Hv, dk, dv, packed != 0, flags, sms);
+}
+
 size_t gdn_workspace_bytes(int B, int T, int Hk, int Hv, int dk, int dv, int packed) {
   if (check_sizes(B, T, Hk, Hv, dk, dv) != GDN_OK) return 0;
   return ws_bytes_for(B, T, Hv, packed);
@@ -181,15 +356,18 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_ARG;
   void* ws = nullptr;
+  ScanPlan plan;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevBuffers& d = g_dev[dev];
     rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hv, cu_seqlens != nullptr));
     if (rc != GDN_OK) return rc;
     ws = d.ws;
+    rc = prepare_scan(dev, B, T, Hv, dk, dv, cu_seqlens != nullptr, 0u, static_cast<cudaStream_t>(stream), plan);
+    if (rc != GDN_OK) return rc;
   }
   return launch_all(q, k, v, g, beta, cu_seqlens, init_state, out, final_state, B, T, Hk, Hv, dk, dv,
-                    static_cast<cudaStream_t>(stream), ws);
+                    static_cast<cudaStream_t>(stream), ws, 0, &plan);
 }
 
 int gdn_prefill_ws(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -240,7 +418,9 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
                    const int32_t* cu_seqlens, const float* init_state, void* out, float* final_state, int B,
                    int T, int Hk, int Hv, int dk, int dv, unsigned flags, void* stream) {
   t_last_cuda_error = 0;
-  if ((flags & ~(unsigned)GDN_FLAG_L2NORM_QK) != 0) return GDN_ERR_ARG;
+  const unsigned known = GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u;
+  if ((flags & ~known) != 0) return GDN_ERR_ARG;
+  if ((flags & GDN_FLAG_TWO_LEVEL) && (flags & GDN_FLAG_ONE_LEVEL)) return GDN_ERR_ARG;
   int rc = check_sizes(B, T, Hk, Hv, dk, dv);
   if (rc != GDN_OK) return rc;
   if (B == 0) return GDN_OK;
@@ -256,15 +436,18 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_ARG;
   void* ws = nullptr;
+  ScanPlan plan;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevBuffers& d = g_dev[dev];
     rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hv, cu_seqlens != nullptr));
     if (rc != GDN_OK) return rc;
     ws = d.ws;
+    rc = prepare_scan(dev, B, T, Hv, dk, dv, cu_seqlens != nullptr, flags, static_cast<cudaStream_t>(stream), plan);
+    if (rc != GDN_OK) return rc;
   }
   return launch_all(q, k, v, g, beta, cu_seqlens, init_state, out, final_state, B, T, Hk, Hv, dk, dv,
-                    static_cast<cudaStream_t>(stream), ws, (flags & GDN_FLAG_L2NORM_QK) ? 1 : 0);
+                    static_cast<cudaStream_t>(stream), ws, (flags & GDN_FLAG_L2NORM_QK) ? 1 : 0, &plan);
 }
 
 int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -292,6 +475,8 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
   if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_ARG;
   unsigned char* base = nullptr;
   void* ws = nullptr;
+  ScanPlan plan;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevBuffers& d = g_dev[dev];
@@ -301,8 +486,9 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
     if (rc != GDN_OK) return rc;
     base = static_cast<unsigned char*>(d.stage);
     ws = d.ws;
+    rc = prepare_scan(dev, B, T, Hv, dk, dv, cu_seqlens != nullptr, 0u, st, plan);
+    if (rc != GDN_OK) return rc;
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const void* src[7] = {q, k, v, g, beta, cu_seqlens, init_state};
   for (int i = 0; i < 7; ++i) {
     if (sz[i] == 0 || src[i] == nullptr) continue;
@@ -313,7 +499,7 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
   rc = launch_all(P(0), P(1), P(2), static_cast<const float*>(P(3)), static_cast<const float*>(P(4)),
                   cu_seqlens ? static_cast<const int32_t*>(P(5)) : nullptr,
                   init_state ? static_cast<const float*>(P(6)) : nullptr, P(7),
-                  final_state ? static_cast<float*>(P(8)) : nullptr, B, T, Hk, Hv, dk, dv, st, ws);
+                  final_state ? static_cast<float*>(P(8)) : nullptr, B, T, Hk, Hv, dk, dv, st, ws, 0, &plan);
   if (rc != GDN_OK) return rc;
   if (nv) {
     e = cudaMemcpyAsync(out, P(7), nv, cudaMemcpyDeviceToHost, st);
@@ -374,6 +560,10 @@ void gdn_release_workspace(void) {
   cudaDeviceSynchronize();
   if (d.ws) cudaFree(d.ws);
   if (d.stage) cudaFree(d.stage);
+  if (d.scan) cudaFree(d.scan);
+  if (d.fork) cudaEventDestroy(d.fork);
+  if (d.join) cudaEventDestroy(d.join);
+  if (d.aux) cudaStreamDestroy(d.aux);
   d = DevBuffers();
 }
 

@@ -1,0 +1,130 @@
+// Two-level chunk scan for long prompts with few heads (sm_103a).
+//
+// Within one (sequence, value head) every row s of the state evolves by the same
+// affine map: with the row-vector form s_t = a_t s_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T
+// of S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T (the recurrence of the
+// "chunked Gated DeltaNet prefill", "Open-Jev-27B-v1.1 native text worker" page,
+// "Validation and optimization scope"), a stretch of tokens maps a start state
+// to S_end = S_start Phi + N.  Phi is that stretch's product of the
+// a_t (I - b_t k_t k_t^T); N is the end state reached from a zero start.  So a
+// long sequence is cut into P segments (on 64-token chunk boundaries), and:
+//
+//   pass A  every segment runs the chunk-sequential state carry twice, at once:
+//           from its start state (the true initial state for segment 0, zero for
+//           the others) giving N_p, and with v = 0 from the identity giving Phi_p;
+//   combine S_start(1) = N_0,  S_start(p + 1) = S_start(p) Phi_p + N_p   (this file);
+//   pass C  every segment runs again from S_start(p), giving the outputs and, for
+//           the last segment, the final state.
+//
+// Passes A and C are the ordinary state-carry kernel run on the segments as packed
+// sequences; this file holds the segment set-up and the fp32 combine.  The serial
+// depth drops from T / 64 chunk steps to about 2 T / (64 P), at about three times
+// the state-carry work -- a gain when the unsegmented problem leaves most SMs idle.
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+namespace {
+constexpr int kSegThreads = 256;
+constexpr int kCombineRows = 8;  // state rows per combine CTA
+}  // namespace
+
+// Segment boundaries and the two start-state sets of pass A.
+//   cu_seg[i] = b T + min(p L, T) for i = b P + p (i = B P gives B T), L = chunks_per_seg * 64;
+//   a_init[(b P + p, h)] = init[(b, h)] for p = 0 (zeros without init), zeros otherwise;
+//   i_init[(b P + p, h)] = the dk x dk identity.
+// grid: B * P * Hv CTAs.
+__global__ void __launch_bounds__(kSegThreads)
+gdn_seg_setup_kernel(const float* __restrict__ init, float* __restrict__ a_init, float* __restrict__ i_init,
+                     int32_t* __restrict__ cu_seg, int B, int T, int P, int chunks_per_seg, int Hv, int DV,
+                     int DK) {
+  const int seg = blockIdx.x / Hv, h = blockIdx.x - seg * Hv;
+  const int b = seg / P, p = seg - b * P;
+  const size_t n_s = (size_t)DV * DK, n_i = (size_t)DK * DK;
+  float4* dst = reinterpret_cast<float4*>(a_init + ((size_t)seg * Hv + h) * n_s);
+  const float4* src = (p == 0 && init != nullptr)
+                          ? reinterpret_cast<const float4*>(init + ((size_t)b * Hv + h) * n_s)
+                          : nullptr;
+  for (size_t e = threadIdx.x; e < n_s / 4; e += kSegThreads)
+    dst[e] = src != nullptr ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+  float* id = i_init + ((size_t)seg * Hv + h) * n_i;
+  for (size_t e = threadIdx.x; e < n_i; e += kSegThreads) id[e] = (e / DK == e % DK) ? 1.f : 0.f;
+  if (blockIdx.x == 0) {
+    const long long seg_len = (long long)chunks_per_seg * kChunk;
+    for (int i = threadIdx.x; i <= B * P; i += kSegThreads) {
+      const int bb = i / P, pp = i - bb * P;
+      const long long off = (long long)pp * seg_len;
+      cu_seg[i] = (int32_t)((long long)bb * T + (off < T ? off : T));
+    }
+  }
+}
+
+// c_init[(b P + p, h)] = S_start(p): the initial state for p = 0, N_0 for p = 1, then
+// S_start(p + 1) = S_start(p) Phi_p + N_p in fp32.  One CTA per (b, h, 8-row slice):
+// thread (j, rg) forms column j of rows 4 rg .. 4 rg + 3.
+// grid: (B * Hv, DV / 8).
+__global__ void __launch_bounds__(kSegThreads)
+gdn_seg_combine_kernel(const float* __restrict__ init, const float* __restrict__ n_fin,
+                       const float* __restrict__ phi, float* __restrict__ c_init, int B, int P, int Hv, int DV,
+                       int DK) {
+  __shared__ float srow[kCombineRows][128];
+  const int b = blockIdx.x / Hv, h = blockIdx.x - b * Hv;
+  const int r0 = blockIdx.y * kCombineRows;
+  const int j = threadIdx.x & 127, rg = threadIdx.x >> 7;
+  const bool col = j < DK;
+  const size_t n_s = (size_t)DV * DK, n_i = (size_t)DK * DK;
+  auto state = [&](const float* base, int p) { return base + (((size_t)b * P + p) * Hv + h) * n_s; };
+  auto state_out = [&](int p) { return c_init + (((size_t)b * P + p) * Hv + h) * n_s; };
+  // S_start(0)
+  {
+    float* dst = c_init + (((size_t)b * P) * Hv + h) * n_s;
+    const float* src = init != nullptr ? init + ((size_t)b * Hv + h) * n_s : nullptr;
+    for (int r = 4 * rg; r < 4 * rg + 4; ++r)
+      if (col) dst[(size_t)(r0 + r) * DK + j] = src != nullptr ? src[(size_t)(r0 + r) * DK + j] : 0.f;
+  }
+  if (P < 2) return;
+  // S_start(1) = N_0
+  for (int r = 4 * rg; r < 4 * rg + 4; ++r) {
+    const float x = col ? state(n_fin, 0)[(size_t)(r0 + r) * DK + j] : 0.f;
+    srow[r][j] = x;
+    if (col) state_out(1)[(size_t)(r0 + r) * DK + j] = x;
+  }
+  __syncthreads();
+  for (int p = 1; p + 1 < P; ++p) {
+    const float* ph = phi + (((size_t)b * P + p) * Hv + h) * n_i;
+    const float* nf = state(n_fin, p);
+    float acc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] = col ? nf[(size_t)(r0 + 4 * rg + u) * DK + j] : 0.f;
+    if (col) {
+      for (int kk = 0; kk < DK; ++kk) {
+        const float f = ph[(size_t)kk * DK + j];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] = fmaf(srow[4 * rg + u][kk], f, acc[u]);
+      }
+    }
+    __syncthreads();  // every thread has read the previous rows
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      srow[4 * rg + u][j] = acc[u];
+      if (col) state_out(p + 1)[(size_t)(r0 + 4 * rg + u) * DK + j] = acc[u];
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_seg_setup(const float* init, float* a_init, float* i_init, int32_t* cu_seg, int B, int T, int P,
+                             int chunks_per_seg, int Hv, int DV, int DK, cudaStream_t st) {
+  gdn_seg_setup_kernel<<<(unsigned)(B * P * Hv), kSegThreads, 0, st>>>(init, a_init, i_init, cu_seg, B, T, P,
+                                                                      chunks_per_seg, Hv, DV, DK);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seg_combine(const float* init, const float* n_fin, const float* phi, float* c_init, int B,
+                               int P, int Hv, int DV, int DK, cudaStream_t st) {
+  dim3 grid((unsigned)(B * Hv), (unsigned)(DV / kCombineRows));
+  gdn_seg_combine_kernel<<<grid, kSegThreads, 0, st>>>(init, n_fin, phi, c_init, B, P, Hv, DV, DK);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -6,7 +6,7 @@ turns tensors into pointers.  There is no fallback: if the library cannot be loa
 
 Functions keep the C names: ``gdn_prefill``, ``gdn_prefill_host``,
 ``gdn_abi_version``, ``gdn_strerror``, ``gdn_last_cuda_error``,
-``gdn_workspace_bytes``, ``gdn_release_workspace``.  ``prefill`` is a convenience
+``gdn_workspace_bytes``, ``gdn_scan_segments``, ``gdn_release_workspace``.  ``prefill`` is a convenience
 wrapper that allocates the outputs with PyTorch and checks the status.
 """
 
@@ -26,13 +26,21 @@ GDN_ERR_LAUNCH = -4
 GDN_ERR_SCRATCH = -5
 GDN_STATIC_SCRATCH_BYTES = 64 << 20
 GDN_FLAG_L2NORM_QK = 1
+GDN_FLAG_TWO_LEVEL = 2
+GDN_FLAG_ONE_LEVEL = 4
 GDN_STATUS_MMA_TIMEOUT = 1
 GDN_STATUS_LOAD_TIMEOUT = 2
 GDN_STATUS_PREP_LOAD_TIMEOUT = 4
 
+
+def GDN_FLAG_SEGMENTS(n: int) -> int:
+    """Segment count for GDN_FLAG_TWO_LEVEL, in flag bits 8..15."""
+    return (int(n) & 0xFF) << 8
+
+
 EXPORTED = ("gdn_abi_version", "gdn_strerror", "gdn_last_cuda_error", "gdn_prefill",
             "gdn_prefill_host", "gdn_prefill_static", "gdn_prefill_ws", "gdn_prefill_ex", "gdn_decode",
-            "gdn_set_phase_events", "gdn_workspace_bytes", "gdn_release_workspace",
+            "gdn_set_phase_events", "gdn_workspace_bytes", "gdn_scan_segments", "gdn_release_workspace",
             "gdn_device_status", "gdn_selftest_wait_timeout")
 
 _lock = threading.Lock()
@@ -86,6 +94,8 @@ def load(build_if_missing: bool = False):
         lib.gdn_last_cuda_error.restype = i
         lib.gdn_workspace_bytes.argtypes = [i] * 7
         lib.gdn_workspace_bytes.restype = ctypes.c_size_t
+        lib.gdn_scan_segments.argtypes = [i] * 7 + [ctypes.c_uint]
+        lib.gdn_scan_segments.restype = i
         lib.gdn_set_phase_events.argtypes = [vp, vp, vp]
         lib.gdn_set_phase_events.restype = None
         lib.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -135,6 +145,11 @@ def gdn_last_cuda_error() -> int:
 
 def gdn_workspace_bytes(B, T, Hk, Hv, dk, dv, packed) -> int:
     return load().gdn_workspace_bytes(B, T, Hk, Hv, dk, dv, int(bool(packed)))
+
+
+def gdn_scan_segments(B, T, Hk, Hv, dk, dv, packed, flags=0) -> int:
+    """Segments per sequence gdn_prefill(_ex) would use on the current device (1 = single-level)."""
+    return load().gdn_scan_segments(B, T, Hk, Hv, dk, dv, int(bool(packed)), int(flags))
 
 
 def gdn_set_phase_events(ev_begin, ev_mid, ev_end) -> None:
@@ -199,7 +214,7 @@ def gdn_prefill_ws(q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
 
 def gdn_prefill_ex(q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
                    B, T, Hk, Hv, dk, dv, flags, stream=None) -> int:
-    """gdn_prefill with option flags (GDN_FLAG_L2NORM_QK); returns the status."""
+    """gdn_prefill with option flags (GDN_FLAG_*); returns the status."""
     return load().gdn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
                                  _ptr(init_state), _ptr(out), _ptr(final_state),
                                  int(B), int(T), int(Hk), int(Hv), int(dk), int(dv), int(flags),

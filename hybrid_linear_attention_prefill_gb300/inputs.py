@@ -180,6 +180,10 @@ WORKLOADS = {
     "varlen32_hk16_hv32": dict(lengths=("uniform", 32, 200, 4096), Hk=16, Hv=32, dk=128, dv=128),
     "t16381_hk16_hv32_carry": dict(B=1, T=16381, Hk=16, Hv=32, dk=128, dv=128,
                                    g_scale=0.1, init_std=0.02),
+    # the maximum prompt with few heads per GPU (heads split over GPUs), where the
+    # chunk-sequential carry alone would leave most SMs idle
+    "t16384_hk4_hv4_carry": dict(B=1, T=16384, Hk=4, Hv=4, dk=128, dv=128,
+                                 g_scale=0.1, init_std=0.02),
 }
 
 HEADLINE = "t4096_hk16_hv32"

@@ -31,7 +31,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 1
+#define GDN_ABI_VERSION 2
 
 /* Status codes (0 = success, negative = error). */
 #define GDN_OK 0
@@ -43,6 +43,10 @@ extern "C" {
 
 /* Flags of gdn_prefill_ex. */
 #define GDN_FLAG_L2NORM_QK 1u /* normalise q and k per token inside the kernels: x / max(||x||, 1e-6) */
+#define GDN_FLAG_TWO_LEVEL 2u /* use the two-level chunk scan (dense batches only) */
+#define GDN_FLAG_ONE_LEVEL 4u /* never use the two-level chunk scan */
+/* Segments per sequence for GDN_FLAG_TWO_LEVEL (2..255; 0 or absent = chosen by the library). */
+#define GDN_FLAG_SEGMENTS(n) ((((unsigned)(n)) & 0xffu) << 8)
 
 /* Size of the fixed device scratch array behind gdn_prefill_static (64 MiB per device). */
 #define GDN_STATIC_SCRATCH_BYTES (64u << 20)
@@ -83,6 +87,19 @@ int gdn_last_cuda_error(void);
  * first call that needs more; about 16 KB per 64-token chunk and value head).
  * After a call at the largest size, later calls allocate nothing.
  *
+ * Long prompts with few heads.  The chunks of a sequence are processed in order,
+ * so a dense batch (cu_seqlens == NULL) whose B * Hv * dv / 32 state-carry blocks
+ * leave most SMs idle is cut into P segments on 64-token boundaries and run as a
+ * two-level scan instead: every segment's state transition and zero-start end
+ * state at once, a short fp32 combine of the segment start states, then every
+ * segment again from its true start state.  This applies when at least three
+ * segments of four or more chunks fit one wave of B * P * Hv * (dv + dk) / 32
+ * blocks (for example one 16,384-token prompt with 4 value heads of 128).  It
+ * uses a second library-owned buffer (two bf16 [Ttot, Hv, dk] tensors and a few
+ * fp32 state sets, also grow-only) and a library-owned second stream joined back
+ * into `stream` by events.  Its results agree with the single-level path to the
+ * stated tolerances, not bit for bit.  gdn_prefill_ex can force or forbid it.
+ *
  * Returns GDN_OK, or an error code before anything is launched (argument and
  * alignment errors), or GDN_ERR_LAUNCH / GDN_ERR_ALLOC.  B == 0 returns GDN_OK
  * and does nothing.  The call does not synchronise the stream.
@@ -116,8 +133,13 @@ int gdn_prefill_host(const void *q, const void *k, const void *v,
  * as a separate fused "norm ... QK" operation before the prefill; "Open-Jev-27B-v1.1
  * native text worker", "Validation and optimization scope").  The norms are summed
  * in fp32 from the bf16 inputs and applied as row scalings of the fp32 products, so
- * no normalised copy of q or k is written.  Unknown flag bits are GDN_ERR_ARG.
- * Everything else as gdn_prefill.
+ * no normalised copy of q or k is written.
+ *
+ * GDN_FLAG_TWO_LEVEL: use the two-level chunk scan described under gdn_prefill
+ * whenever the batch is dense and has at least two chunks per sequence, with
+ * GDN_FLAG_SEGMENTS(n) segments per sequence (capped at the chunk count) or, without
+ * it, the library's choice (at least 3).  GDN_FLAG_ONE_LEVEL: never use it.  Both
+ * together, or unknown flag bits, are GDN_ERR_ARG.  Everything else as gdn_prefill.
  */
 int gdn_prefill_ex(const void *q, const void *k, const void *v,
                    const float *g, const float *beta,
@@ -137,7 +159,8 @@ int gdn_prefill_ex(const void *q, const void *k, const void *v,
  * the same buffers -- the calling convention behind the pages' per-prompt-length
  * CUDA Graph replay ("Cua-S1 4B 0.2 native text worker", CUDA Graph paragraph).
  * Returns GDN_ERR_SCRATCH when the workspace is too small, GDN_ERR_ALIGN when it
- * is not 256-byte aligned.
+ * is not 256-byte aligned.  Always the single-level path (no second stream, no
+ * library buffers).
  */
 int gdn_prefill_ws(const void *q, const void *k, const void *v,
                    const float *g, const float *beta,
@@ -191,6 +214,7 @@ void gdn_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end);
  *     the caller must order them.
  *   - The first call on each device looks the array's address up (with that device
  *     current); make that first call before capturing the stream into a CUDA graph.
+ *   - Always the single-level path (no two-level scan).
  */
 int gdn_prefill_static(const void *q, const void *k, const void *v,
                        const float *g, const float *beta,
@@ -225,6 +249,11 @@ int gdn_device_status(int *status);
  * fault.
  */
 int gdn_selftest_wait_timeout(int max_polls, int *status);
+
+/* Segments per sequence that gdn_prefill_ex with these flags (gdn_prefill: flags = 0)
+ * would use on the current device: 1 for the single-level path, P >= 2 for the
+ * two-level chunk scan.  0 on bad arguments or unknown flags. */
+int gdn_scan_segments(int B, int T, int Hk, int Hv, int dk, int dv, int packed, unsigned flags);
 
 /* Bytes of device workspace gdn_prefill needs for these sizes (0 on bad arguments). */
 size_t gdn_workspace_bytes(int B, int T, int Hk, int Hv, int dk, int dv, int packed);

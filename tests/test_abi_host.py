@@ -116,5 +116,15 @@ def test_decode_argument_checks(lib):
 def test_prefill_ex_rejects_unknown_flags(lib):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, cu_seqlens=None, init_state=None,
              out=FAKE, final_state=None, B=1, T=64, Hk=1, Hv=1, dk=128, dv=128, stream=0)
-    assert gdn.gdn_prefill_ex(**a, flags=2) == gdn.GDN_ERR_ARG
-    assert gdn.gdn_prefill_ex(**{**a, "B": 0}, flags=gdn.GDN_FLAG_L2NORM_QK) == gdn.GDN_OK
+    for bad in (8, 1 << 16, 1 << 31, gdn.GDN_FLAG_TWO_LEVEL | gdn.GDN_FLAG_ONE_LEVEL):
+        assert gdn.gdn_prefill_ex(**a, flags=bad) == gdn.GDN_ERR_ARG
+    for ok in (gdn.GDN_FLAG_L2NORM_QK, gdn.GDN_FLAG_TWO_LEVEL | gdn.GDN_FLAG_SEGMENTS(5), gdn.GDN_FLAG_ONE_LEVEL):
+        assert gdn.gdn_prefill_ex(**{**a, "B": 0}, flags=ok) == gdn.GDN_OK
+
+
+def test_segment_flag_encoding():
+    """GDN_FLAG_SEGMENTS(n) occupies bits 8..15, as the header defines it."""
+    hdr = open(HEADER).read()
+    assert "#define GDN_FLAG_SEGMENTS(n) ((((unsigned)(n)) & 0xffu) << 8)" in hdr
+    assert gdn.GDN_FLAG_SEGMENTS(3) == 3 << 8 and gdn.GDN_FLAG_SEGMENTS(255) == 0xFF00
+    assert (gdn.GDN_FLAG_TWO_LEVEL, gdn.GDN_FLAG_ONE_LEVEL) == (2, 4)
