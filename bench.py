@@ -354,8 +354,8 @@ def run_gpu_arm(args):
             "ms_per_step_min": min(step_ms), "wall_s": round(wall, 3),
             "cpu_baseline": cpu, "e2e": e2e,
             # prep + state carry (+ chunk table when packed); the two-level scan adds the
-            # segment set-up, its chunk table, a second pass-A carry, the combine and pass C
-            "gpu_launches": K * (2 + (inp.cu_seqlens is not None) if segs == 1 else 7),
+            # segment set-up, a second pass-A carry, the combine and pass C
+            "gpu_launches": K * (2 + (inp.cu_seqlens is not None) if segs == 1 else 6),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

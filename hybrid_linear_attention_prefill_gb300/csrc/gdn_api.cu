@@ -22,7 +22,8 @@ cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*,
                             const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
                             int, long long, int, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
-cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int, int, int, int, int, int, int, cudaStream_t);
+cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int32_t*, int, int, int, int, int, int, int,
+                             cudaStream_t);
 cudaError_t launch_seg_combine(const float*, const float*, const float*, float*, int, int, int, int, int,
                                cudaStream_t);
 template <int DK>
@@ -104,22 +105,25 @@ int ensure(void*& ptr, size_t& have, size_t need) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---- two-level chunk scan (dense batches with few heads and many chunks) -----------
-// Number of segments P (1 = the single-level path).  Pass A runs B P Hv (dv + dk) / 32
-// state-carry CTAs at once, so P is what fits one wave on the device's SMs, at least
-// 3 (with 2 the two passes take as long as one unsegmented pass) and at most one
-// segment per 4 chunks.
+// Number of segments P (1 = the single-level path).  Pass A runs, at once, the
+// zero-start carry of segments 0 .. B P - 2 (dv / 32 CTAs per head each) and the
+// transition carry of segments 1 .. B P - 2 (dk / 32 per head), so P is the largest
+// count whose pass A fits one wave on the device's SMs -- at least 3 (with 2 the two
+// passes take as long as one unsegmented pass) and at most one segment per 8 chunks.
 int choose_segments(int B, int T, int Hv, int dk, int dv, bool packed, unsigned flags, int sms) {
   if (packed || (flags & GDN_FLAG_ONE_LEVEL) != 0 || B <= 0 || T <= 0) return 1;
   const long long nc = (T + gdn::kChunk - 1) / gdn::kChunk;
-  const long long per_seg = std::max<long long>(1, (long long)B * Hv * (dv + dk) / 32);
-  const long long fit = sms / per_seg;
+  // Hv ((B P - 1) dv + (B P - 2) dk) / 32 <= sms
+  const long long fit = ((long long)sms * 32 / std::max(Hv, 1) + dv + 2LL * dk) / ((long long)B * (dv + dk));
   const int req = (int)((flags >> 8) & 0xffu);
   if ((flags & GDN_FLAG_TWO_LEVEL) != 0) {
     long long P = req >= 2 ? req : std::max<long long>(3, fit);
     P = std::min(P, nc);
     return P >= 2 ? (int)P : 1;
   }
-  long long P = std::min<long long>(std::min<long long>(fit, nc / 4), 32);
+  // segments of at least 8 chunks, so the two passes beat one by more than the
+  // set-up and combine cost
+  long long P = std::min<long long>(std::min<long long>(fit, nc / 8), 32);
   return P >= 3 ? (int)P : 1;
 }
 
@@ -253,23 +257,34 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     float* c_init = reinterpret_cast<float*>(sb + L.c_init);
     float* f_fin = reinterpret_cast<float*>(sb + L.f_fin);
     const int ttot = B * T;
-    if ((e = gdn::launch_seg_setup(init, a_init, i_init, cu_seg, B, T, P, cps, Hv, dv, dk, st)) != cudaSuccess ||
-        (e = gdn::launch_chunk_table(cu_seg, BP, ttot, off_seg, st)) != cudaSuccess ||
+    if ((e = gdn::launch_seg_setup(init, a_init, i_init, cu_seg, off_seg, B, T, P, cps, Hv, dv, dk, st)) !=
+            cudaSuccess ||
         (e = cudaEventRecord(plan->fork, st)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(plan->aux, plan->fork, 0)) != cudaSuccess)
       return set_cuda_error(e, GDN_ERR_LAUNCH);
-    // pass A: transition matrices (v = 0 from the identity, dk rows) beside the zero-start runs
-    if ((e = chain_dk(dk, q, k, vzero, g, beta, cu_seg, off_seg, tiles, i_init, oscr, phi, err, BP, ttot, Hk,
-                      Hv, dk, nc_dense, nslots, norm_qk, plan->aux)) != cudaSuccess ||
-        (e = chain_dk(dk, q, k, v, g, beta, cu_seg, off_seg, tiles, a_init, out, n_fin, err, BP, ttot, Hk, Hv,
+    // Each run below covers a contiguous range [first, first + n) of the segment list,
+    // passed as a packed batch of n sequences by offsetting cu_seg, off_seg and the
+    // per-sequence init / final-state pointers.  Segments a run does not need (the
+    // last of each sequence in the zero-start run, the first in pass C, ...) are left
+    // out wherever they sit at the ends of the list.
+    const size_t ps = (size_t)Hv * dv * dk, pi = (size_t)Hv * dk * dk;
+    // pass A: zero-start runs of segments 0 .. BP-2 (segment 0 of each sequence from the
+    // true initial state: its outputs are final) beside the transition runs of 1 .. BP-2
+    // (v = 0 from the identity, dk rows) on the second stream
+    if (BP - 2 >= 1 &&
+        (e = chain_dk(dk, q, k, vzero, g, beta, cu_seg + 1, off_seg + 1, tiles, i_init + pi, oscr, phi + pi, err,
+                      BP - 2, ttot, Hk, Hv, dk, nc_dense, nslots, norm_qk, plan->aux)) != cudaSuccess)
+      return set_cuda_error(e, GDN_ERR_LAUNCH);
+    if ((e = chain_dk(dk, q, k, v, g, beta, cu_seg, off_seg, tiles, a_init, out, n_fin, err, BP - 1, ttot, Hk, Hv,
                       dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess ||
         (e = cudaEventRecord(plan->join, plan->aux)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(st, plan->join, 0)) != cudaSuccess)
       return set_cuda_error(e, GDN_ERR_LAUNCH);
-    // segment start states, then pass C from them (outputs; the last segment's final state)
+    // segment start states, then pass C over segments 1 .. BP-1 (the outputs; the last
+    // segment's final state)
     if ((e = gdn::launch_seg_combine(init, n_fin, phi, c_init, B, P, Hv, dv, dk, st)) != cudaSuccess ||
-        (e = chain_dk(dk, q, k, v, g, beta, cu_seg, off_seg, tiles, c_init, out, f_fin, err, BP, ttot, Hk, Hv,
-                      dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess)
+        (e = chain_dk(dk, q, k, v, g, beta, cu_seg + 1, off_seg + 1, tiles, c_init + ps, out, f_fin + ps, err,
+                      BP - 1, ttot, Hk, Hv, dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess)
       return set_cuda_error(e, GDN_ERR_LAUNCH);
     if (fin != nullptr) {
       const size_t per = (size_t)Hv * dv * dk;

@@ -26,104 +26,140 @@ namespace gdn {
 
 namespace {
 constexpr int kSegThreads = 256;
-constexpr int kCombineRows = 8;  // state rows per combine CTA
+constexpr int kSetupSplit = 8;    // CTAs per (segment, head) in the set-up
+constexpr int kCombineRows = 4;   // state rows per combine CTA
+constexpr int kCombineThreads = 128;
+constexpr int kPhiTile = 32;      // rows of Phi per shared-memory tile
 }  // namespace
 
-// Segment boundaries and the two start-state sets of pass A.
+// Segment boundaries, their chunk slots, and the two start-state sets of pass A.
 //   cu_seg[i] = b T + min(p L, T) for i = b P + p (i = B P gives B T), L = chunks_per_seg * 64;
+//   off_seg[i] = b nc + min(p chunks_per_seg, nc): the slot of the segment's first chunk in
+//                the unsegmented (dense) chunk numbering the preparation kernel used;
 //   a_init[(b P + p, h)] = init[(b, h)] for p = 0 (zeros without init), zeros otherwise;
 //   i_init[(b P + p, h)] = the dk x dk identity.
-// grid: B * P * Hv CTAs.
+// grid: (B * P * Hv, kSetupSplit); each CTA writes one row band of both states.
 __global__ void __launch_bounds__(kSegThreads)
 gdn_seg_setup_kernel(const float* __restrict__ init, float* __restrict__ a_init, float* __restrict__ i_init,
-                     int32_t* __restrict__ cu_seg, int B, int T, int P, int chunks_per_seg, int Hv, int DV,
-                     int DK) {
+                     int32_t* __restrict__ cu_seg, int32_t* __restrict__ off_seg, int B, int T, int P,
+                     int chunks_per_seg, int Hv, int DV, int DK) {
   const int seg = blockIdx.x / Hv, h = blockIdx.x - seg * Hv;
   const int b = seg / P, p = seg - b * P;
   const size_t n_s = (size_t)DV * DK, n_i = (size_t)DK * DK;
-  float4* dst = reinterpret_cast<float4*>(a_init + ((size_t)seg * Hv + h) * n_s);
-  const float4* src = (p == 0 && init != nullptr)
-                          ? reinterpret_cast<const float4*>(init + ((size_t)b * Hv + h) * n_s)
-                          : nullptr;
-  for (size_t e = threadIdx.x; e < n_s / 4; e += kSegThreads)
-    dst[e] = src != nullptr ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
-  float* id = i_init + ((size_t)seg * Hv + h) * n_i;
-  for (size_t e = threadIdx.x; e < n_i; e += kSegThreads) id[e] = (e / DK == e % DK) ? 1.f : 0.f;
-  if (blockIdx.x == 0) {
+  {
+    const size_t lo = n_s / 4 * blockIdx.y / kSetupSplit, hi = n_s / 4 * (blockIdx.y + 1) / kSetupSplit;
+    float4* dst = reinterpret_cast<float4*>(a_init + ((size_t)seg * Hv + h) * n_s);
+    const float4* src = (p == 0 && init != nullptr)
+                            ? reinterpret_cast<const float4*>(init + ((size_t)b * Hv + h) * n_s)
+                            : nullptr;
+    for (size_t e = lo + threadIdx.x; e < hi; e += kSegThreads)
+      dst[e] = src != nullptr ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  {
+    const size_t lo = n_i * blockIdx.y / kSetupSplit, hi = n_i * (blockIdx.y + 1) / kSetupSplit;
+    float* id = i_init + ((size_t)seg * Hv + h) * n_i;
+    for (size_t e = lo + threadIdx.x; e < hi; e += kSegThreads) id[e] = (e / DK == e % DK) ? 1.f : 0.f;
+  }
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
     const long long seg_len = (long long)chunks_per_seg * kChunk;
+    const int nc = (T + kChunk - 1) / kChunk;
     for (int i = threadIdx.x; i <= B * P; i += kSegThreads) {
       const int bb = i / P, pp = i - bb * P;
       const long long off = (long long)pp * seg_len;
+      const long long c0 = (long long)pp * chunks_per_seg;
       cu_seg[i] = (int32_t)((long long)bb * T + (off < T ? off : T));
+      off_seg[i] = (int32_t)((long long)bb * nc + (c0 < nc ? c0 : nc));
     }
   }
 }
 
 // c_init[(b P + p, h)] = S_start(p): the initial state for p = 0, N_0 for p = 1, then
-// S_start(p + 1) = S_start(p) Phi_p + N_p in fp32.  One CTA per (b, h, 8-row slice):
-// thread (j, rg) forms column j of rows 4 rg .. 4 rg + 3.
-// grid: (B * Hv, DV / 8).
-__global__ void __launch_bounds__(kSegThreads)
+// S_start(p + 1) = S_start(p) Phi_p + N_p in fp32.  One CTA per (b, h, 4-row slice);
+// thread j forms column j of the 4 rows.  Phi_p streams through shared memory in
+// 32-row tiles (cp.async, double-buffered), so every thread reads it once.
+// grid: (B * Hv, DV / 4).
+__global__ void __launch_bounds__(kCombineThreads)
 gdn_seg_combine_kernel(const float* __restrict__ init, const float* __restrict__ n_fin,
                        const float* __restrict__ phi, float* __restrict__ c_init, int B, int P, int Hv, int DV,
                        int DK) {
   __shared__ float srow[kCombineRows][128];
+  __shared__ __align__(16) float tile[2][kPhiTile][128];
   const int b = blockIdx.x / Hv, h = blockIdx.x - b * Hv;
   const int r0 = blockIdx.y * kCombineRows;
-  const int j = threadIdx.x & 127, rg = threadIdx.x >> 7;
+  const int j = threadIdx.x;
   const bool col = j < DK;
   const size_t n_s = (size_t)DV * DK, n_i = (size_t)DK * DK;
   auto state = [&](const float* base, int p) { return base + (((size_t)b * P + p) * Hv + h) * n_s; };
   auto state_out = [&](int p) { return c_init + (((size_t)b * P + p) * Hv + h) * n_s; };
   // S_start(0)
   {
-    float* dst = c_init + (((size_t)b * P) * Hv + h) * n_s;
     const float* src = init != nullptr ? init + ((size_t)b * Hv + h) * n_s : nullptr;
-    for (int r = 4 * rg; r < 4 * rg + 4; ++r)
-      if (col) dst[(size_t)(r0 + r) * DK + j] = src != nullptr ? src[(size_t)(r0 + r) * DK + j] : 0.f;
+#pragma unroll
+    for (int r = 0; r < kCombineRows; ++r)
+      if (col) state_out(0)[(size_t)(r0 + r) * DK + j] = src != nullptr ? src[(size_t)(r0 + r) * DK + j] : 0.f;
   }
   if (P < 2) return;
   // S_start(1) = N_0
-  for (int r = 4 * rg; r < 4 * rg + 4; ++r) {
+#pragma unroll
+  for (int r = 0; r < kCombineRows; ++r) {
     const float x = col ? state(n_fin, 0)[(size_t)(r0 + r) * DK + j] : 0.f;
     srow[r][j] = x;
     if (col) state_out(1)[(size_t)(r0 + r) * DK + j] = x;
   }
-  __syncthreads();
+  const int ntiles = DK / kPhiTile;
+  const int per_row = DK / 4;  // 16-byte pieces per Phi row
+  auto load_tile = [&](const float* ph, int t, int buf) {
+    for (int e = threadIdx.x; e < kPhiTile * per_row; e += kCombineThreads) {
+      const int r = e / per_row, c4 = e - r * per_row;
+      cp_async16(&tile[buf][r][4 * c4], ph + (size_t)(t * kPhiTile + r) * DK + 4 * c4, true);
+    }
+    cp_async_commit();
+  };
   for (int p = 1; p + 1 < P; ++p) {
     const float* ph = phi + (((size_t)b * P + p) * Hv + h) * n_i;
     const float* nf = state(n_fin, p);
-    float acc[4];
+    float acc[kCombineRows];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[u] = col ? nf[(size_t)(r0 + 4 * rg + u) * DK + j] : 0.f;
-    if (col) {
-      for (int kk = 0; kk < DK; ++kk) {
-        const float f = ph[(size_t)kk * DK + j];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) acc[u] = fmaf(srow[4 * rg + u][kk], f, acc[u]);
+    for (int u = 0; u < kCombineRows; ++u) acc[u] = col ? nf[(size_t)(r0 + u) * DK + j] : 0.f;
+    load_tile(ph, 0, 0);
+    for (int t = 0; t < ntiles; ++t) {
+      if (t + 1 < ntiles) {
+        load_tile(ph, t + 1, (t + 1) & 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
       }
-    }
-    __syncthreads();  // every thread has read the previous rows
+      __syncthreads();  // tile t (and, at t = 0, the previous rows in srow) visible
+      if (col) {
+#pragma unroll 8
+        for (int kk = 0; kk < kPhiTile; ++kk) {
+          const float f = tile[t & 1][kk][j];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      srow[4 * rg + u][j] = acc[u];
-      if (col) state_out(p + 1)[(size_t)(r0 + 4 * rg + u) * DK + j] = acc[u];
+          for (int u = 0; u < kCombineRows; ++u) acc[u] = fmaf(srow[u][t * kPhiTile + kk], f, acc[u]);
+        }
+      }
+      __syncthreads();  // tile t read before it is refilled
     }
-    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kCombineRows; ++u) {
+      srow[u][j] = acc[u];
+      if (col) state_out(p + 1)[(size_t)(r0 + u) * DK + j] = acc[u];
+    }
   }
 }
 
-cudaError_t launch_seg_setup(const float* init, float* a_init, float* i_init, int32_t* cu_seg, int B, int T, int P,
-                             int chunks_per_seg, int Hv, int DV, int DK, cudaStream_t st) {
-  gdn_seg_setup_kernel<<<(unsigned)(B * P * Hv), kSegThreads, 0, st>>>(init, a_init, i_init, cu_seg, B, T, P,
-                                                                      chunks_per_seg, Hv, DV, DK);
+cudaError_t launch_seg_setup(const float* init, float* a_init, float* i_init, int32_t* cu_seg, int32_t* off_seg,
+                             int B, int T, int P, int chunks_per_seg, int Hv, int DV, int DK, cudaStream_t st) {
+  dim3 grid((unsigned)(B * P * Hv), kSetupSplit);
+  gdn_seg_setup_kernel<<<grid, kSegThreads, 0, st>>>(init, a_init, i_init, cu_seg, off_seg, B, T, P,
+                                                     chunks_per_seg, Hv, DV, DK);
   return cudaGetLastError();
 }
 
 cudaError_t launch_seg_combine(const float* init, const float* n_fin, const float* phi, float* c_init, int B,
                                int P, int Hv, int DV, int DK, cudaStream_t st) {
   dim3 grid((unsigned)(B * Hv), (unsigned)(DV / kCombineRows));
-  gdn_seg_combine_kernel<<<grid, kSegThreads, 0, st>>>(init, n_fin, phi, c_init, B, P, Hv, DV, DK);
+  gdn_seg_combine_kernel<<<grid, kCombineThreads, 0, st>>>(init, n_fin, phi, c_init, B, P, Hv, DV, DK);
   return cudaGetLastError();
 }
 

@@ -119,7 +119,9 @@ def test_chosen_automatically_for_a_long_prompt_with_few_heads(gdn):
     """16,384 tokens with 4 value heads: gdn_prefill takes the two-level path on its own
     (bitwise the forced result with the library's segment count) and matches the oracle."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    P = min(sms // (1 * 4 * (128 + 128) // 32), 16384 // 64 // 4, 32)
+    # the largest P whose pass A -- 4 heads x ((P - 1) x 4 + (P - 2) x 4) CTAs -- fits one wave
+    P = min((sms * 32 // 4 + 128 + 2 * 128) // (128 + 128), 16384 // 64 // 8, 32)
+    assert gdn.gdn_scan_segments(1, 16384, 4, 4, 128, 128, 0) == (P if P >= 3 else 1)
     if P < 3:
         pytest.skip("device too small for the automatic choice")
     inp = make_gdn_inputs(B=1, T=16384, Hk=4, Hv=4, dk=128, dv=128, seed=102, g_scale=0.1, init_std=0.02)
