@@ -273,18 +273,34 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
     // ---- A (fp32) and P (bf16), 8 columns at a time, lower triangle only ----------
     // Gamma[t][i] = 2^(gamma2_t - gamma2_i) with gamma2 = gamma log2(e): the exponent
-    // is never positive for i <= t.
+    // is never positive for i <= t.  A thread keeps one 8-column block (the CTA size is
+    // a multiple of 8), so its gamma and 1/||k|| columns are loaded once.
+    static_assert(kPrepThreads % 8 == 0, "column block fixed per thread");
+    const int c8 = (tid & 7) * 8;
+    float gcol[8], rcol[8];
+    {
+      const float4 g0 = *reinterpret_cast<const float4*>(gam + c8), g1 = *reinterpret_cast<const float4*>(gam + c8 + 4);
+      const float4 r0 = *reinterpret_cast<const float4*>(rnk + c8), r1 = *reinterpret_cast<const float4*>(rnk + c8 + 4);
+      gcol[0] = g0.x; gcol[1] = g0.y; gcol[2] = g0.z; gcol[3] = g0.w;
+      gcol[4] = g1.x; gcol[5] = g1.y; gcol[6] = g1.z; gcol[7] = g1.w;
+      rcol[0] = r0.x; rcol[1] = r0.y; rcol[2] = r0.z; rcol[3] = r0.w;
+      rcol[4] = r1.x; rcol[5] = r1.y; rcol[6] = r1.z; rcol[7] = r1.w;
+    }
     for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
-      const int t = e >> 3, c8 = (e & 7) * 8;
+      const int t = e >> 3;
       float av[8], pv[8];
       if (c8 <= t) {
         const float gt = gam[t], bt = bet[t] * rnk[t], qt = rnq[t];
-        const float* gk = Gs + t * LDF + c8;
-        const float* gq = Gs + kChunk * LDF + t * LDF + c8;
+        const float4 k0 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8);
+        const float4 k1 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8 + 4);
+        const float4 q0 = *reinterpret_cast<const float4*>(Gs + kChunk * LDF + t * LDF + c8);
+        const float4 q1 = *reinterpret_cast<const float4*>(Gs + kChunk * LDF + t * LDF + c8 + 4);
+        const float gk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        const float gq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int i = c8 + u;
-          const float dcy = i <= t ? exp2f(gt - gam[i]) * rnk[i] : 0.f;
+          const float dcy = i <= t ? exp2f(gt - gcol[u]) * rcol[u] : 0.f;
           pv[u] = qt * dcy * gq[u];
           av[u] = i < t ? bt * dcy * gk[u] : 0.f;
         }
@@ -330,22 +346,18 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     __syncthreads();
 
     // ---- merge 16 -> 32: T[o+16.., o..] = -T22 (A21 T11), o = 0 and 32 -------
-    if (warp < 2) {
-      const int o = 32 * warp;
-      float* W = Wt + 16 * warp * LDW;  // this warp's 16 x 16 part of the buffer
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3(acc, As, LDF, o + 16, o, Tms, LDF, o, o + 8 * nt, lane);
-        store_tile(W, LDW, 0, 8 * nt, acc, 1.f, lane);
-      }
+    // Warp w < 4 forms the 8-column tile nt = w % 2 of block o = 32 (w / 2): its column
+    // tile of W = A21 T11 is all that its tile of T21 = -T22 W needs.
+    if (warp < 4) {
+      const int o = 32 * (warp >> 1), nt = warp & 1;
+      float* W = Wt + 16 * (warp >> 1) * LDW;  // this block's 16 x 16 part of the buffer
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f32x3(acc, As, LDF, o + 16, o, Tms, LDF, o, o + 8 * nt, lane);
+      store_tile(W, LDW, 0, 8 * nt, acc, 1.f, lane);
       __syncwarp();
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3(acc, Tms, LDF, o + 16, o + 16, W, LDW, 0, 8 * nt, lane);
-        store_tile(Tms, LDF, o + 16, o + 8 * nt, acc, -1.f, lane);
-      }
+      float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f32x3(acc2, Tms, LDF, o + 16, o + 16, W, LDW, 0, 8 * nt, lane);
+      store_tile(Tms, LDF, o + 16, o + 8 * nt, acc2, -1.f, lane);
     }
     __syncthreads();
 
