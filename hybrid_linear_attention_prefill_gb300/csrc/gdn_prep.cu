@@ -18,12 +18,12 @@
 //
 // One CTA (8 warps) handles one chunk slot and one key head, and loops over the
 // value heads that share the key head, so the Grams K K^T and Q K^T are computed
-// once per key head.  The inverse is blocked: the four 16 x 16 diagonal blocks
-// by forward substitution in fp32, then the 16 -> 32 -> 64 merges
-// T21 = -T22 A21 T11 as tensor-core products whose fp32 operands are split into
-// bf16 hi + lo parts (hi*hi + hi*lo + lo*hi, ~2^-16 relative).  Only non-positive
-// exponents are ever taken (gamma_t - gamma_i, i <= t), so nothing overflows
-// however strong the decay.
+// once per key head (one tcgen05 product in TMEM).  The inverse is blocked: the
+// four 16 x 16 diagonal blocks by forward substitution in fp32, then the
+// 16 -> 32 -> 64 merges T21 = -T22 A21 T11 as tensor-core products whose fp32
+// operands are split into bf16 hi + lo parts (hi*hi + hi*lo + lo*hi, ~2^-16
+// relative).  Only non-positive exponents are ever taken (gamma_t - gamma_i,
+// i <= t), so nothing overflows however strong the decay.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -85,7 +85,7 @@ struct PrepSmem {
   static constexpr int offRN = offGam + 2 * kChunk * 4;  // inverse norms of k rows, then q rows
   static constexpr int offGB = offRN + 2 * kChunk * 4;   // [2 buffers][g 64 | beta 64] fp32
   static constexpr int offBar = offGB + 2 * 2 * kChunk * 4;
-  static constexpr int bytes = offBar + 16 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int bytes = offBar + 32 + 1024;  // 2 mbarriers + TMEM base; + slack for 1024-byte alignment
 };
 
 template <int DK>
@@ -108,7 +108,8 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   float* Wt = reinterpret_cast<float*>(smem + L::offW);  // [32][LDW]
   float* gam = reinterpret_cast<float*>(smem + L::offGam);
   float* bet = gam + kChunk;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::offBar);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::offBar);  // [0] tiles loaded, [1] Grams done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offBar + 16);
   float* gbuf = reinterpret_cast<float*>(smem + L::offGB);
   float* rnk = reinterpret_cast<float*>(smem + L::offRN);  // 1/||k_t|| (1 without normalisation)
   float* rnq = rnk + kChunk;                                // 1/||q_t||
@@ -149,20 +150,29 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   };
   prefetch_gb(0, 0);
 
-  // ---- load the K and Q tiles by TMA (tokens past the end of the tensor are zero)
+  // ---- TMEM for the Grams; the K and Q tiles by TMA (tokens past the end are zero)
   constexpr int kKBlocks = DK > 64 ? 2 : 1;
+  constexpr uint32_t kGramCols = 64;
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, kGramCols);
+    tc::tmem_relinquish();
+  }
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
     tc::fence_mbar_init();
-    tc::mbar_arrive_expect_tx(bar, 2 * kKBlocks * 8192);
+    tc::mbar_arrive_expect_tx(&bar[0], 2 * kKBlocks * 8192);
 #pragma unroll
     for (int db = 0; db < kKBlocks; ++db) {
-      tc::tma_load_3d(KQ + db * 16384, &tm_k, 64 * db, hk, (int)t0, bar);
-      tc::tma_load_3d(KQ + db * 16384 + 8192, &tm_q, 64 * db, hk, (int)t0, bar);
+      tc::tma_load_3d(KQ + db * 16384, &tm_k, 64 * db, hk, (int)t0, &bar[0]);
+      tc::tma_load_3d(KQ + db * 16384 + 8192, &tm_q, 64 * db, hk, (int)t0, &bar[0]);
     }
   }
+  tc::fence_before();
   __syncthreads();
-  if (!tc::mbar_wait(bar, 0, 1u << 24)) atomicOr(err, 4);
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (!tc::mbar_wait(&bar[0], 0, 1u << 24)) atomicOr(err, 4);
   // rows t >= n belong to the next sequence (or are past the end): clear them
   if (n < kChunk) {
     for (int e = tid; e < kKBlocks * 2 * (kChunk - n) * 8; e += kPrepThreads) {
@@ -171,80 +181,44 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       *reinterpret_cast<uint4*>(KQ + db * 16384 + tc::sw128(64 * which + r, piece)) = make_uint4(0, 0, 0, 0);
     }
   }
+  tc::fence_proxy_async();  // the cleared rows are read by the tensor core
   __syncthreads();
 
-  // ---- Grams: G0 = K K^T, G1 = Q K^T on the lower block triangle ------------
-  // Warp roles: matrix (K or Q rows), m-tile pair {0,3} or {1,2} (10 n-tiles each),
-  // and which half of the dk range; the second half is added into the first.
-  {
-    const int mat = warp & 1, pairsel = (warp >> 1) & 1, khalf = warp >> 2;
-    float* Gd = Gs + mat * kChunk * LDF;
-    const int m = lane >> 3;
-    constexpr int KS = DK / 16;
-    constexpr int KH = KS / 2 > 0 ? KS / 2 : 1;
-    float acc[2][8][4];
+  // ---- Grams on the tensor core: D = [K; Q] K^T (M = 128, N = 64, K = dk) -------
+  // Rows 0..63 of D are K K^T, rows 64..127 Q K^T; both operands are the K-major
+  // swizzled tile as loaded (the B operand is its first 64 rows).
+  if (tid == 0) {
+    tc::fence_after();
+    constexpr uint32_t kID = tc::idesc_bf16(128, 64, 0, 0);
+    const uint32_t kq = smem_u32(KQ);
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[u][i][0] = acc[u][i][1] = acc[u][i][2] = acc[u][i][3] = 0.f;
-#pragma unroll
-    for (int kq = 0; kq < KH; ++kq) {
-      const int kk = khalf * KH + kq;
-      if (kk < KS) {
-        const int db = kk >> 2, c0 = 2 * (kk & 3);  // 16-byte piece of the 128 B row
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int mi = pairsel == 0 ? (u == 0 ? 0 : 3) : (u == 0 ? 1 : 2);
-          uint32_t a[4];
-          const int ra = 64 * mat + 16 * mi + 8 * (m & 1) + (lane & 7);
-          ldsm_x4(a, KQ + db * 16384 + tc::sw128(ra, c0 + (m >> 1)));
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            if (p <= mi) {
-              uint32_t bb[4];
-              const int rb = 8 * (2 * p + (m >> 1)) + (lane & 7);
-              ldsm_x4(bb, KQ + db * 16384 + tc::sw128(rb, c0 + (m & 1)));
-              mma_bf16(acc[u][2 * p], a, bb[0], bb[1]);
-              mma_bf16(acc[u][2 * p + 1], a, bb[2], bb[3]);
-            }
-          }
-        }
-      }
+    for (int ks = 0; ks < DK / 16; ++ks) {
+      const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+      tc::mma_bf16(tmem, tc::sdesc(kq + off, 16, 1024, tc::kSw128), tc::sdesc(kq + off, 16, 1024, tc::kSw128), kID,
+                   ks > 0);
     }
-    // first k half stores, second k half adds
-#pragma unroll
-    for (int phase = 0; phase < 2; ++phase) {
-      if (phase == khalf) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int mi = pairsel == 0 ? (u == 0 ? 0 : 3) : (u == 0 ? 1 : 2);
-#pragma unroll
-          for (int nj = 0; nj < 8; ++nj) {
-            if (nj <= 2 * mi + 1) {
-              const int g8 = lane >> 2, tg = lane & 3;
-              float* d0 = Gd + (16 * mi + g8) * LDF + 8 * nj + 2 * tg;
-              float* d1 = d0 + 8 * LDF;
-              if (phase == 0) {
-                *reinterpret_cast<float2*>(d0) = make_float2(acc[u][nj][0], acc[u][nj][1]);
-                *reinterpret_cast<float2*>(d1) = make_float2(acc[u][nj][2], acc[u][nj][3]);
-              } else {
-                d0[0] += acc[u][nj][0]; d0[1] += acc[u][nj][1];
-                d1[0] += acc[u][nj][2]; d1[1] += acc[u][nj][3];
-              }
-            }
-          }
-        }
-      }
-      __syncthreads();
-    }
+    tc::commit(&bar[1]);
   }
-
-  // inverse norms of the k and q rows, read before the K/Q tiles are overwritten
+  // inverse norms of the k and q rows while the product runs
   if (tid < 2 * kChunk) {
     const float r = norm_qk ? tc::inv_norm(tc::row_sumsq_sw128<DK>(KQ, (tid & 63) + 64 * (tid >> 6))) : 1.f;
     rnk[tid] = r;  // tid 0..63: k rows, 64..127: q rows (rnq = rnk + 64)
   }
-  __syncthreads();
+  if (!tc::mbar_wait(&bar[1], 0, 1u << 24)) atomicOr(err, 4);
+  tc::fence_after();
+  // TMEM -> the fp32 Grams: warp w reads lanes 32 (w % 4) .. +31 (rows: 0..63 K, 64..127
+  // Q) and columns 32 (w / 4) .. +31
+  {
+    const int q4 = warp & 3, hf = warp >> 2;
+    float v[32];
+    tc::tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + 32 * hf, v);
+    float* dst = Gs + (q4 >> 1) * kChunk * LDF + (32 * (q4 & 1) + lane) * LDF + 32 * hf;
+#pragma unroll
+    for (int p = 0; p < 8; ++p)
+      *reinterpret_cast<float4*>(dst + 4 * p) = make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
+  }
+  tc::fence_before();
+  __syncthreads();  // Grams and norms visible; the tiles are dead from here on (A and Tm overwrite them)
 
   for (int gi = 0; gi < G; ++gi) {
     const int h = hk * G + gi;
@@ -437,6 +411,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     __syncthreads();
   }
+  if (warp == 0) tc::tmem_dealloc(tmem, kGramCols);
 }
 
 // Prefix sums of chunk counts for packed sequences: chunk_off[b] = sum over
