@@ -15,12 +15,12 @@
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, int*, int, int, int, int, int, int, int, cudaStream_t);
+                        void*, int*, int, int, int, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
                             const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
-                            int, long long, int, cudaStream_t);
+                            int, long long, int, int, int, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int32_t*, int, int, int, int, int, int, int,
                              cudaStream_t);
@@ -46,7 +46,13 @@ struct DevBuffers {
   cudaStream_t aux = nullptr;  // second stream for pass A's transition run
   cudaEvent_t fork = nullptr, join = nullptr;
   int sms = 0;
+  // gdn_prefill_host's copy / compute pipeline over head groups
+  bool pipe_ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp[3] = {nullptr, nullptr, nullptr};
+  cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[4] = {}, ev_done[4] = {};
 };
+
+constexpr int kMaxHostGroups = 4;
 
 std::mutex g_mu;
 DevBuffers g_dev[kMaxDevices];
@@ -199,7 +205,7 @@ cudaError_t chain(const void* q, const void* k, const void* v, const float* g, c
                   float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots,
                   int norm_qk, cudaStream_t st) {
   return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, DV,
-                                  nc_dense, nslots, norm_qk, st);
+                                  nc_dense, nslots, norm_qk, 0, Hv, st);
 }
 
 cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -213,9 +219,15 @@ cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const 
   }
 }
 
+// The prefill for value heads [h0, h1) (all heads when h1 < 0; h0 and h1 multiples of
+// Hv / Hk) on `st`.  `table` = false skips the packed chunk table (already built).
 int launch_all(const void* q, const void* k, const void* v, const float* g, const float* beta,
                const int32_t* cu, const float* init, void* out, float* fin, int B, int T, int Hk, int Hv,
-               int dk, int dv, cudaStream_t st, void* ws, int norm_qk = 0, const ScanPlan* plan = nullptr) {
+               int dk, int dv, cudaStream_t st, void* ws, int norm_qk = 0, const ScanPlan* plan = nullptr,
+               int h0 = 0, int h1 = -1, bool table = true) {
+  if (h1 < 0) h1 = Hv;
+  const int G = Hv / Hk;
+  const int hk0 = h0 / G, nhk = (h1 - h0) / G;
   const int packed = cu != nullptr;
   int* err = static_cast<int*>(ws);
   int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + 256);
@@ -223,7 +235,7 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   const long long nslots = num_slots(B, T, packed);
   cudaError_t e = cudaSuccess;
-  if (packed) {
+  if (packed && table) {
     e = gdn::launch_chunk_table(cu, B, T, chunk_off, st);
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
@@ -233,14 +245,14 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   if (nslots > 0) {
     if (nslots > 0x7fffffffLL) return GDN_ERR_ARG;
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
     }
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
   if (ev[1] != nullptr && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
-  if (plan != nullptr && plan->P > 1 && !packed && nslots > 0) {
+  if (plan != nullptr && plan->P > 1 && !packed && nslots > 0 && h0 == 0 && h1 == Hv) {
     // ---- two-level scan over P segments per sequence (see gdn_scan.cu) ----------------
     const int P = plan->P, BP = B * P;
     const int cps = (nc_dense + P - 1) / P;  // chunks per segment
@@ -298,9 +310,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     return GDN_OK;
   }
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
   }
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
@@ -492,9 +504,16 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
   void* ws = nullptr;
   ScanPlan plan;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DevBuffers* dp = nullptr;
+  // Head groups: the copies of group i + 1 overlap the kernels of group i (each group on
+  // its own stream, so the latency-bound state carries of all groups run side by side)
+  // and the copy-out of earlier groups.  Whole key heads per group; one group for small
+  // problems or with the two-level scan.
+  int ngroups = 1;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevBuffers& d = g_dev[dev];
+    dp = &d;
     rc = ensure(d.stage, d.stage_bytes, total);
     if (rc != GDN_OK) return rc;
     rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hv, cu_seqlens != nullptr));
@@ -503,29 +522,110 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
     ws = d.ws;
     rc = prepare_scan(dev, B, T, Hv, dk, dv, cu_seqlens != nullptr, 0u, st, plan);
     if (rc != GDN_OK) return rc;
+    if (plan.P <= 1 && nq + nv >= ((size_t)8 << 20)) ngroups = std::min(kMaxHostGroups, Hk);
+    if (ngroups > 1 && !d.pipe_ready) {
+      e = cudaStreamCreateWithFlags(&d.h2d, cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.d2h, cudaStreamNonBlocking);
+      for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&d.comp[i], cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_start, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_end, cudaEventDisableTiming);
+      for (int i = 0; i < kMaxHostGroups && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&d.ev_in[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_done[i], cudaEventDisableTiming);
+      }
+      if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+      d.pipe_ready = true;
+    }
   }
+  auto P = [&](int i) -> unsigned char* { return sz[i] ? base + off[i] : nullptr; };
   const void* src[7] = {q, k, v, g, beta, cu_seqlens, init_state};
-  for (int i = 0; i < 7; ++i) {
-    if (sz[i] == 0 || src[i] == nullptr) continue;
-    e = cudaMemcpyAsync(base + off[i], src[i], sz[i], cudaMemcpyHostToDevice, st);
+  if (ngroups <= 1) {
+    for (int i = 0; i < 7; ++i) {
+      if (sz[i] == 0 || src[i] == nullptr) continue;
+      e = cudaMemcpyAsync(base + off[i], src[i], sz[i], cudaMemcpyHostToDevice, st);
+      if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+    }
+    rc = launch_all(P(0), P(1), P(2), reinterpret_cast<const float*>(P(3)), reinterpret_cast<const float*>(P(4)),
+                    cu_seqlens ? reinterpret_cast<const int32_t*>(P(5)) : nullptr,
+                    init_state ? reinterpret_cast<const float*>(P(6)) : nullptr, P(7),
+                    final_state ? reinterpret_cast<float*>(P(8)) : nullptr, B, T, Hk, Hv, dk, dv, st, ws, 0, &plan);
+    if (rc != GDN_OK) return rc;
+    if (nv) {
+      e = cudaMemcpyAsync(out, P(7), nv, cudaMemcpyDeviceToHost, st);
+      if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+    }
+    if (final_state) {
+      e = cudaMemcpyAsync(final_state, P(8), ns, cudaMemcpyDeviceToHost, st);
+      if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+    }
+    e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+    return GDN_OK;
   }
-  auto P = [&](int i) -> void* { return sz[i] ? base + off[i] : nullptr; };
-  rc = launch_all(P(0), P(1), P(2), static_cast<const float*>(P(3)), static_cast<const float*>(P(4)),
-                  cu_seqlens ? static_cast<const int32_t*>(P(5)) : nullptr,
-                  init_state ? static_cast<const float*>(P(6)) : nullptr, P(7),
-                  final_state ? static_cast<float*>(P(8)) : nullptr, B, T, Hk, Hv, dk, dv, st, ws, 0, &plan);
-  if (rc != GDN_OK) return rc;
-  if (nv) {
-    e = cudaMemcpyAsync(out, P(7), nv, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+
+  // ---- pipelined over head groups --------------------------------------------------
+  DevBuffers& d = *dp;
+  const int G = Hv / Hk;
+  auto check = [&](cudaError_t x) { return x == cudaSuccess ? GDN_OK : set_cuda_error(x, GDN_ERR_LAUNCH); };
+  auto h2d_cols = [&](int i, size_t col0, size_t width, size_t pitch, size_t rows) {  // column band of a row-major array
+    return cudaMemcpy2DAsync(base + off[i] + col0, pitch, static_cast<const unsigned char*>(src[i]) + col0, pitch,
+                             width, rows, cudaMemcpyHostToDevice, d.h2d);
+  };
+  // the copies start after everything already queued on `stream` (earlier calls use the same staging)
+  if ((rc = check(cudaEventRecord(d.ev_start, st))) != GDN_OK ||
+      (rc = check(cudaStreamWaitEvent(d.h2d, d.ev_start, 0))) != GDN_OK)
+    return rc;
+  // small, whole: cu_seqlens (and the packed chunk table), g, beta
+  if (cu_seqlens != nullptr) {
+    if ((rc = check(cudaMemcpyAsync(P(5), cu_seqlens, ncu, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK) return rc;
+    int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + 256);
+    if ((rc = check(gdn::launch_chunk_table(reinterpret_cast<const int32_t*>(P(5)), B, T, chunk_off, d.h2d))) !=
+        GDN_OK)
+      return rc;
   }
-  if (final_state) {
-    e = cudaMemcpyAsync(final_state, P(8), ns, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  if ((rc = check(cudaMemcpyAsync(P(3), g, ng, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK ||
+      (rc = check(cudaMemcpyAsync(P(4), beta, ng, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK)
+    return rc;
+  int hk_lo[kMaxHostGroups + 1];
+  for (int i = 0; i <= ngroups; ++i) hk_lo[i] = (int)((long long)Hk * i / ngroups);
+  for (int i = 0; i < ngroups; ++i) {
+    const size_t k0 = (size_t)hk_lo[i], k1 = (size_t)hk_lo[i + 1];
+    const size_t h0 = k0 * G, h1 = k1 * G;
+    // inputs of group i: the key heads' q / k columns, the value heads' v columns, the init slices
+    if ((rc = check(h2d_cols(0, k0 * dk * 2, (k1 - k0) * dk * 2, (size_t)Hk * dk * 2, ntok))) != GDN_OK ||
+        (rc = check(h2d_cols(1, k0 * dk * 2, (k1 - k0) * dk * 2, (size_t)Hk * dk * 2, ntok))) != GDN_OK ||
+        (rc = check(h2d_cols(2, h0 * dv * 2, (h1 - h0) * dv * 2, (size_t)Hv * dv * 2, ntok))) != GDN_OK)
+      return rc;
+    if (init_state != nullptr &&
+        (rc = check(h2d_cols(6, h0 * dv * dk * 4, (h1 - h0) * dv * dk * 4, (size_t)Hv * dv * dk * 4, B))) != GDN_OK)
+      return rc;
+    if ((rc = check(cudaEventRecord(d.ev_in[i], d.h2d))) != GDN_OK) return rc;
+    // kernels of group i on their own stream
+    cudaStream_t cs = i == 0 ? st : d.comp[i - 1];
+    if ((rc = check(cudaStreamWaitEvent(cs, d.ev_in[i], 0))) != GDN_OK) return rc;
+    rc = launch_all(P(0), P(1), P(2), reinterpret_cast<const float*>(P(3)), reinterpret_cast<const float*>(P(4)),
+                    cu_seqlens ? reinterpret_cast<const int32_t*>(P(5)) : nullptr,
+                    init_state ? reinterpret_cast<const float*>(P(6)) : nullptr, P(7),
+                    final_state ? reinterpret_cast<float*>(P(8)) : nullptr, B, T, Hk, Hv, dk, dv, cs, ws, 0, nullptr,
+                    (int)h0, (int)h1, false);
+    if (rc != GDN_OK) return rc;
+    if ((rc = check(cudaEventRecord(d.ev_done[i], cs))) != GDN_OK) return rc;
+    // outputs of group i back to the host
+    if ((rc = check(cudaStreamWaitEvent(d.d2h, d.ev_done[i], 0))) != GDN_OK ||
+        (rc = check(cudaMemcpy2DAsync(static_cast<unsigned char*>(out) + h0 * dv * 2, (size_t)Hv * dv * 2,
+                                      P(7) + h0 * dv * 2, (size_t)Hv * dv * 2, (h1 - h0) * dv * 2, ntok,
+                                      cudaMemcpyDeviceToHost, d.d2h))) != GDN_OK)
+      return rc;
+    if (final_state != nullptr &&
+        (rc = check(cudaMemcpy2DAsync(reinterpret_cast<unsigned char*>(final_state) + h0 * dv * dk * 4,
+                                      (size_t)Hv * dv * dk * 4, P(8) + h0 * dv * dk * 4, (size_t)Hv * dv * dk * 4,
+                                      (h1 - h0) * dv * dk * 4, B, cudaMemcpyDeviceToHost, d.d2h))) != GDN_OK)
+      return rc;
   }
-  e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  if ((rc = check(cudaEventRecord(d.ev_end, d.d2h))) != GDN_OK ||
+      (rc = check(cudaStreamWaitEvent(st, d.ev_end, 0))) != GDN_OK ||
+      (rc = check(cudaStreamSynchronize(st))) != GDN_OK)
+    return rc;
   return GDN_OK;
 }
 
@@ -579,6 +679,17 @@ void gdn_release_workspace(void) {
   if (d.fork) cudaEventDestroy(d.fork);
   if (d.join) cudaEventDestroy(d.join);
   if (d.aux) cudaStreamDestroy(d.aux);
+  if (d.pipe_ready) {
+    cudaStreamDestroy(d.h2d);
+    cudaStreamDestroy(d.d2h);
+    for (cudaStream_t c : d.comp) cudaStreamDestroy(c);
+    cudaEventDestroy(d.ev_start);
+    cudaEventDestroy(d.ev_end);
+    for (int i = 0; i < kMaxHostGroups; ++i) {
+      cudaEventDestroy(d.ev_in[i]);
+      cudaEventDestroy(d.ev_done[i]);
+    }
+  }
   d = DevBuffers();
 }
 

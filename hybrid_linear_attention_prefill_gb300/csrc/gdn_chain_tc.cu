@@ -128,7 +128,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu,
                     const int32_t* __restrict__ chunk_off, const float* init, __nv_bfloat16* __restrict__ out,
                     float* fin, int* __restrict__ err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
-                    long long nslots, int norm_qk) {
+                    long long nslots, int norm_qk, int h_base) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
@@ -148,7 +148,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int ntiles = DV / kDVT;
   const int b = blockIdx.x / ntiles;
   const int dv0 = (blockIdx.x - b * ntiles) * kDVT;
-  const int h = blockIdx.y;
+  const int h = h_base + (int)blockIdx.y;
   const int hk = h / (Hv / Hk);
   const float scale = rsqrtf((float)DK);
   constexpr int kP1 = DK / 16 < kParts ? DK / 16 : kParts;  // partials used by phase 1
@@ -453,7 +453,7 @@ template <int DK>
 cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const int32_t* cu, const int32_t* chunk_off, const void* ws, const float* init,
                             void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
-                            long long nslots, int norm_qk, cudaStream_t st) {
+                            long long nslots, int norm_qk, int h_base, int h_count, cudaStream_t st) {
   const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
   const cuuint64_t tt = (cuuint64_t)(ttot > 0 ? ttot : 1);
   CUtensorMap mk, mq, mv, mw;
@@ -480,18 +480,18 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
   }
   cudaError_t e = set_smem_limit_once<gdn_chain_tc_kernel<DK>>(kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)B * (DV / kDVT), Hv);
+  dim3 grid((unsigned)B * (DV / kDVT), h_count);  // value heads h_base .. h_base + h_count - 1
   gdn_chain_tc_kernel<DK><<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, init,
                                                                static_cast<__nv_bfloat16*>(out), fin, err, B, T,
-                                                               Hk, Hv, DV, nc_dense, nslots, norm_qk);
+                                                               Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base);
   return cudaGetLastError();
 }
 
 #define GDN_INST_CHAIN_TC(DK)                                                                                \
   template cudaError_t launch_chain_tc<DK>(const void*, const void*, const void*, const float*, const float*, \
                                            const int32_t*, const int32_t*, const void*, const float*, void*,  \
-                                           float*, int*, int, int, int, int, int, int, long long, int,        \
-                                           cudaStream_t);
+                                           float*, int*, int, int, int, int, int, int, long long, int, int,   \
+                                           int, cudaStream_t);
 GDN_INST_CHAIN_TC(32)
 GDN_INST_CHAIN_TC(64)
 GDN_INST_CHAIN_TC(128)

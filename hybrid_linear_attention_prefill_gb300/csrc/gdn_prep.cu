@@ -94,7 +94,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 const float* __restrict__ g, const float* __restrict__ beta,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_off,
                 __nv_bfloat16* __restrict__ ws, int* __restrict__ err, int B, int T, int Hk, int Hv,
-                int nc_dense, int norm_qk) {
+                int nc_dense, int norm_qk, int hk_base) {
   using L = PrepSmem<DK>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -115,7 +115,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   float* rnq = rnk + kChunk;                                // 1/||q_t||
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slot = blockIdx.x, hk = blockIdx.y;
+  const int slot = blockIdx.x, hk = hk_base + (int)blockIdx.y;
 
   // ---- which sequence and chunk this slot is ---------------------------------
   int b, c;
@@ -476,7 +476,8 @@ PFN_cuTensorMapEncodeTiled_v12000 prep_map_encoder() {
 template <int DK>
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const float* beta,
                         const int32_t* cu, const int32_t* chunk_off, void* ws, int* err, int B, int T,
-                        int Hk, int Hv, int nslots, int nc_dense, int norm_qk, cudaStream_t st) {
+                        int Hk, int Hv, int nslots, int nc_dense, int norm_qk, int hk_base, int hk_count,
+                        cudaStream_t st) {
   using L = PrepSmem<DK>;
   PFN_cuTensorMapEncodeTiled_v12000 enc = prep_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -494,10 +495,10 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_limit_once<gdn_prep_kernel<DK>>(L::bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(nslots, Hk);
+  dim3 grid(nslots, hk_count);  // key heads hk_base .. hk_base + hk_count - 1
   gdn_prep_kernel<DK><<<grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
                                                            static_cast<__nv_bfloat16*>(ws), err, B, T, Hk, Hv,
-                                                           nc_dense, norm_qk);
+                                                           nc_dense, norm_qk, hk_base);
   return cudaGetLastError();
 }
 
@@ -508,7 +509,8 @@ cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_o
 
 #define GDN_INST_PREP(DK)                                                                                  \
   template cudaError_t launch_prep<DK>(const void*, const void*, const float*, const float*, const int32_t*, \
-                                       const int32_t*, void*, int*, int, int, int, int, int, int, int, cudaStream_t);
+                                       const int32_t*, void*, int*, int, int, int, int, int, int, int, int, int,  \
+                                       cudaStream_t);
 GDN_INST_PREP(32)
 GDN_INST_PREP(64)
 GDN_INST_PREP(128)

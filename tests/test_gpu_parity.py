@@ -218,6 +218,37 @@ def test_host_entry_matches_device_entry():
     assert np.array_equal(bf16_bits_to_f32(out), o_dev) and np.array_equal(fin, s_dev)
 
 
+@pytest.mark.parametrize("case", [
+    dict(B=1, T=4096, Hk=4, Hv=8, dk=128, dv=128, init_std=0.1),            # 4 head groups, dense
+    dict(lengths=[1500, 0, 2600, 77], Hk=3, Hv=6, dk=128, dv=64, init_std=0.1),  # 3 groups, packed
+    dict(B=2, T=3000, Hk=8, Hv=8, dk=64, dv=128),                             # no initial state
+])
+def test_host_entry_pipelined_over_head_groups(case):
+    """Large enough for gdn_prefill_host to overlap its copies with the kernels of head
+    groups on separate streams: bitwise the device entry's results, pinned or pageable."""
+    import torch
+    from hybrid_linear_attention_prefill_gb300 import gdn
+    from hybrid_linear_attention_prefill_gb300.inputs import bf16_bits_to_f32
+
+    inp = make_gdn_inputs(seed=24, **case)
+    o_dev, s_dev = run_gpu(inp)
+    B, Tt = inp.B, inp.total_tokens
+    T = inp.T if inp.cu_seqlens is None else Tt
+    for pin in (True, False):
+        def host(a):
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            return t.pin_memory() if pin else t
+        out = host(np.zeros((Tt, inp.Hv, inp.dv), dtype=np.int16))
+        fin = host(np.zeros((B, inp.Hv, inp.dv, inp.dk), dtype=np.float32))
+        init = None if inp.init is None else host(inp.init)
+        cu = None if inp.cu_seqlens is None else host(inp.cu_seqlens)
+        gdn.check(gdn.gdn_prefill_host(host(inp.q.view(np.int16)), host(inp.k.view(np.int16)),
+                                       host(inp.v.view(np.int16)), host(inp.g), host(inp.beta), cu, init,
+                                       out, fin, B, T, inp.Hk, inp.Hv, inp.dk, inp.dv, 0))
+        o_host = bf16_bits_to_f32(out.numpy().view(np.uint16))
+        assert np.array_equal(o_host, o_dev) and np.array_equal(fin.numpy(), s_dev)
+
+
 def test_misaligned_device_pointer_rejected():
     from gpu_common import dev_inputs
     from hybrid_linear_attention_prefill_gb300 import gdn
