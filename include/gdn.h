@@ -116,7 +116,11 @@ int gdn_prefill(const void *q, const void *k, const void *v,
  * alignment).  Copies the inputs to the library's device staging area, runs
  * gdn_prefill on `stream`, copies out and final_state back and synchronises
  * `stream` before returning.  Page-locked host buffers give the fastest copies.
- * cu_seqlens, init_state and final_state may be NULL as above.
+ * cu_seqlens, init_state and final_state may be NULL as above.  For problems of
+ * 8 MB or more (q, k and v together) the work is split into up to four groups of
+ * whole key heads: the copies of one group overlap the kernels of the previous
+ * one and the copy-back of earlier ones, on library-owned streams that are joined
+ * back into `stream`; the results are bit for bit those of gdn_prefill.
  */
 int gdn_prefill_host(const void *q, const void *k, const void *v,
                      const float *g, const float *beta,
