@@ -28,7 +28,7 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-from hybrid_linear_attention_prefill_gb300.inputs import HEADLINE, WORKLOADS, workload  # noqa: E402
+from hybrid_linear_attention_prefill_gb300.inputs import HEADLINE, WORKLOADS, make_gdn_inputs, workload  # noqa: E402
 
 METRIC = "Gated DeltaNet prefill tokens/s at T=4096,Hv=32; % of GB300 roofline"
 FALLBACK_HBM_GBS = 6800.0
@@ -391,6 +391,114 @@ def measure_e2e(inp, gdn, torch, stream, steps):
 
 
 # ---------------------------------------------------------------------------
+# measurements of the adjacent entry points (one JSON line each, device timing)
+# ---------------------------------------------------------------------------
+def _timed_steps(torch, stream, flush, step, warmup, K):
+    """Mean and min milliseconds of `step` over K calls, L2 flushed before each."""
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return statistics.mean(ms), min(ms)
+
+
+def run_extra_arm(args):
+    """--op decode | --norm-qk | --graph: the one-token step, the in-kernel q/k
+    normalisation and CUDA-graph replay of the caller-workspace entry."""
+    import torch
+
+    from hybrid_linear_attention_prefill_gb300 import build as gbuild
+    from hybrid_linear_attention_prefill_gb300 import gdn
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    gbuild.build()
+    gdn.load()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    peaks = read_peaks()
+    sampler = ClockSampler(0)
+    if args.op == "decode":
+        base = WORKLOADS[args.workload]
+        Hk, Hv, dk, dv, B = base["Hk"], base["Hv"], base["dk"], base["dv"], args.decode_batch
+        inp = make_gdn_inputs(B=B, T=1, Hk=Hk, Hv=Hv, dk=dk, dv=dv, seed=args.seed, init_std=0.05)
+        d = to_device(inp, torch, dev)
+        state = d["init"].clone()
+        out = torch.empty((B, Hv, dv), dtype=torch.bfloat16, device=dev)
+
+        def step():
+            gdn.check(gdn.gdn_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], state, out,
+                                     B, Hk, Hv, dk, dv, stream))
+
+        sampler.start()
+        ms, ms_min = _timed_steps(torch, stream, flush, step, args.warmup, args.steps)
+        clocks = sampler.stop()
+        nbytes = 2 * B * Hv * dv * dk * 4 + B * (2 * Hk * dk + 2 * Hv * dv) * 2 + 2 * B * Hv * 4
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        line = {"metric": "GDN decode tokens/s (one token per sequence, state updated in place)",
+                "value": B / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_min": ms_min, "higher_is_better": True,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"decode_b{B}_hk{Hk}_hv{Hv}", "B": B, "Hk": Hk, "Hv": Hv, "dk": dk,
+                           "dv": dv, "state_bytes": B * Hv * dv * dk * 4,
+                           "l2": "flushed between timed steps (256 MB write)"},
+                "roofline": {"bound": "hbm", "kernel": "gdn_decode_kernel", "achieved": round(achieved, 1),
+                             "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
+                             "traffic": None, "peak_source": peaks["source"]},
+                "gpu_launches": args.steps, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+        return
+    inp = workload(args.workload, seed=args.seed)
+    d = to_device(inp, torch, dev)
+    Tt, B = inp.total_tokens, inp.B
+    out = torch.empty((Tt, inp.Hv, inp.dv), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((B, inp.Hv, inp.dv, inp.dk), dtype=torch.float32, device=dev)
+    args_common = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], d["init"], out, fin,
+                   B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv)
+    mode = "norm_qk" if args.norm_qk else "graph"
+    if args.norm_qk:
+        def step():
+            gdn.check(gdn.gdn_prefill_ex(*args_common, gdn.GDN_FLAG_L2NORM_QK, stream))
+    else:
+        nbytes = gdn.gdn_workspace_bytes(B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, d["cu"] is not None)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):  # shared-memory limits set once, before capture
+            gdn.check(gdn.gdn_prefill_ws(*args_common, ws, nbytes, side))
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            gdn.check(gdn.gdn_prefill_ws(*args_common, ws, nbytes, side))
+
+        def step():
+            graph.replay()
+    sampler.start()
+    ms, ms_min = _timed_steps(torch, stream, flush, step, args.warmup, args.steps)
+    clocks = sampler.stop()
+    alg = algorithmic(inp)
+    t_hbm = alg["total"] / (peaks["hbm"] * 1e9)
+    line = {"metric": METRIC, "value": Tt / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_min": ms_min, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "mode": mode, "B": B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv,
+                       "dk": inp.dk, "dv": inp.dv, "l2": "flushed between timed steps (256 MB write)"},
+            "path_roofline": {"roofline_us": round(t_hbm * 1e6, 2), "bound": "hbm",
+                              "frac": round(t_hbm / (ms * 1e-3), 4)},
+            "gpu_launches": args.steps * (2 + (inp.cu_seqlens is not None)), "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
 # the reference arm: the float64 oracle on the host cores
 # ---------------------------------------------------------------------------
 def run_reference_arm(args):
@@ -446,11 +554,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--levels", choices=["auto", "one", "two"], default="auto",
                     help="chunk scan: the library's choice, single-level only, or two-level")
+    ap.add_argument("--op", choices=["prefill", "decode"], default="prefill",
+                    help="decode: time gdn_decode on --decode-batch sequences of the workload's heads")
+    ap.add_argument("--decode-batch", type=int, default=128)
+    ap.add_argument("--norm-qk", action="store_true", help="time gdn_prefill_ex with GDN_FLAG_L2NORM_QK")
+    ap.add_argument("--graph", action="store_true", help="time gdn_prefill_ws captured into a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference_arm(args)
+    elif args.op == "decode" or args.norm_qk or args.graph:
+        run_extra_arm(args)
     else:
         run_gpu_arm(args)
 
