@@ -15,12 +15,12 @@
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, int*, int, int, int, int, int, int, int, int, int, cudaStream_t);
+                        void*, float*, int*, int, int, int, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
-                            const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
-                            int, long long, int, int, int, cudaStream_t);
+                            const int32_t*, const void*, const float*, const float*, void*, float*, int*, int, int,
+                            int, int, int, int, long long, int, int, int, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int32_t*, int, int, int, int, int, int, int,
                              cudaStream_t);
@@ -77,10 +77,12 @@ long long num_slots(int B, int T, int packed) {
   return (long long)(T + gdn::kChunk - 1) / gdn::kChunk + B;
 }
 
-// Workspace: [256 B status words][chunk table, B + 1 int32, padded to 256 B][Tm/PT tiles]
-size_t ws_bytes_for(int B, int T, int Hv, int packed) {
+// Workspace: [256 B status words][chunk table, B + 1 int32, padded to 256 B]
+//            [Tm/PT tiles per (slot, value head)][inverse q/k norms per (slot, key head)]
+size_t ws_bytes_for(int B, int T, int Hk, int Hv, int packed) {
   const size_t table = align_up(sizeof(int32_t) * ((size_t)B + 1), 256);
-  return 256 + table + (size_t)num_slots(B, T, packed) * Hv * gdn::kWsPerSlotHead;
+  const size_t ns = (size_t)num_slots(B, T, packed);
+  return 256 + table + ns * Hv * gdn::kWsPerSlotHead + ns * Hk * gdn::kWsNormPerSlotKHead;
 }
 
 int set_cuda_error(cudaError_t e, int code) {
@@ -201,21 +203,21 @@ int prepare_scan(int dev, int B, int T, int Hv, int dk, int dv, bool packed, uns
 
 template <int DK>
 cudaError_t chain(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                  const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* init, void* out,
-                  float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots,
-                  int norm_qk, cudaStream_t st) {
-  return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, DV,
-                                  nc_dense, nslots, norm_qk, 0, Hv, st);
+                  const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* ws_rn,
+                  const float* init, void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV,
+                  int nc_dense, long long nslots, int norm_qk, cudaStream_t st) {
+  return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv,
+                                  DV, nc_dense, nslots, norm_qk, 0, Hv, st);
 }
 
 cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const float* g, const float* beta,
-                     const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* init, void* out,
-                     float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots,
-                     int norm_qk, cudaStream_t st) {
+                     const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* ws_rn,
+                     const float* init, void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV,
+                     int nc_dense, long long nslots, int norm_qk, cudaStream_t st) {
   switch (dk) {
-    case 32: return chain<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
-    case 64: return chain<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
-    default: return chain<128>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
+    case 32: return chain<32>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
+    case 64: return chain<64>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
+    default: return chain<128>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
   }
 }
 
@@ -234,6 +236,7 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   void* tiles = static_cast<unsigned char*>(ws) + 256 + align_up(sizeof(int32_t) * ((size_t)B + 1), 256);
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   const long long nslots = num_slots(B, T, packed);
+  float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
   cudaError_t e = cudaSuccess;
   if (packed && table) {
     e = gdn::launch_chunk_table(cu, B, T, chunk_off, st);
@@ -245,9 +248,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   if (nslots > 0) {
     if (nslots > 0x7fffffffLL) return GDN_ERR_ARG;
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
     }
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
@@ -284,10 +287,10 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     // true initial state: its outputs are final) beside the transition runs of 1 .. BP-2
     // (v = 0 from the identity, dk rows) on the second stream
     if (BP - 2 >= 1 &&
-        (e = chain_dk(dk, q, k, vzero, g, beta, cu_seg + 1, off_seg + 1, tiles, i_init + pi, oscr, phi + pi, err,
+        (e = chain_dk(dk, q, k, vzero, g, beta, cu_seg + 1, off_seg + 1, tiles, ws_rn, i_init + pi, oscr, phi + pi, err,
                       BP - 2, ttot, Hk, Hv, dk, nc_dense, nslots, norm_qk, plan->aux)) != cudaSuccess)
       return set_cuda_error(e, GDN_ERR_LAUNCH);
-    if ((e = chain_dk(dk, q, k, v, g, beta, cu_seg, off_seg, tiles, a_init, out, n_fin, err, BP - 1, ttot, Hk, Hv,
+    if ((e = chain_dk(dk, q, k, v, g, beta, cu_seg, off_seg, tiles, ws_rn, a_init, out, n_fin, err, BP - 1, ttot, Hk, Hv,
                       dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess ||
         (e = cudaEventRecord(plan->join, plan->aux)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(st, plan->join, 0)) != cudaSuccess)
@@ -295,7 +298,7 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     // segment start states, then pass C over segments 1 .. BP-1 (the outputs; the last
     // segment's final state)
     if ((e = gdn::launch_seg_combine(init, n_fin, phi, c_init, B, P, Hv, dv, dk, st)) != cudaSuccess ||
-        (e = chain_dk(dk, q, k, v, g, beta, cu_seg + 1, off_seg + 1, tiles, c_init + ps, out, f_fin + ps, err,
+        (e = chain_dk(dk, q, k, v, g, beta, cu_seg + 1, off_seg + 1, tiles, ws_rn, c_init + ps, out, f_fin + ps, err,
                       BP - 1, ttot, Hk, Hv, dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess)
       return set_cuda_error(e, GDN_ERR_LAUNCH);
     if (fin != nullptr) {
@@ -310,9 +313,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     return GDN_OK;
   }
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
   }
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
@@ -360,7 +363,7 @@ int gdn_scan_segments(int B, int T, int Hk, int Hv, int dk, int dv, int packed, 
 
 size_t gdn_workspace_bytes(int B, int T, int Hk, int Hv, int dk, int dv, int packed) {
   if (check_sizes(B, T, Hk, Hv, dk, dv) != GDN_OK) return 0;
-  return ws_bytes_for(B, T, Hv, packed);
+  return ws_bytes_for(B, T, Hk, Hv, packed);
 }
 
 int gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -387,7 +390,7 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevBuffers& d = g_dev[dev];
-    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hv, cu_seqlens != nullptr));
+    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hk, Hv, cu_seqlens != nullptr));
     if (rc != GDN_OK) return rc;
     ws = d.ws;
     rc = prepare_scan(dev, B, T, Hv, dk, dv, cu_seqlens != nullptr, 0u, static_cast<cudaStream_t>(stream), plan);
@@ -414,7 +417,7 @@ int gdn_prefill_ws(const void* q, const void* k, const void* v, const float* g, 
   if (ntok == 0 && final_state == nullptr) return GDN_OK;
   if (workspace == nullptr) return GDN_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGN;
-  if (workspace_bytes < ws_bytes_for(B, T, Hv, cu_seqlens != nullptr)) return GDN_ERR_SCRATCH;
+  if (workspace_bytes < ws_bytes_for(B, T, Hk, Hv, cu_seqlens != nullptr)) return GDN_ERR_SCRATCH;
   return launch_all(q, k, v, g, beta, cu_seqlens, init_state, out, final_state, B, T, Hk, Hv, dk, dv,
                     static_cast<cudaStream_t>(stream), workspace);
 }
@@ -467,7 +470,7 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevBuffers& d = g_dev[dev];
-    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hv, cu_seqlens != nullptr));
+    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hk, Hv, cu_seqlens != nullptr));
     if (rc != GDN_OK) return rc;
     ws = d.ws;
     rc = prepare_scan(dev, B, T, Hv, dk, dv, cu_seqlens != nullptr, flags, static_cast<cudaStream_t>(stream), plan);
@@ -516,7 +519,7 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
     dp = &d;
     rc = ensure(d.stage, d.stage_bytes, total);
     if (rc != GDN_OK) return rc;
-    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hv, cu_seqlens != nullptr));
+    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hk, Hv, cu_seqlens != nullptr));
     if (rc != GDN_OK) return rc;
     base = static_cast<unsigned char*>(d.stage);
     ws = d.ws;

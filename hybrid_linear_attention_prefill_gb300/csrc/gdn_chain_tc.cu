@@ -66,7 +66,9 @@ constexpr int kOffTP = 32768;              // 16384
 constexpr int kOffV = kOffTP + 16384;      // 64 rows x 64 B (64 B swizzle)
 constexpr int kOffG = kOffV + 4096;        // 64 fp32
 constexpr int kOffB = kOffG + 256;         // 64 fp32
+constexpr int kOffRN = kOffB + 256;        // 128 fp32: inverse norms of the k rows, then the q rows
 constexpr int kStage = 54272;              // 53 KB, multiple of 1024
+static_assert(kOffRN + 512 <= kStage, "stage layout");
 // B operands after the two stages
 constexpr int kOffS = 2 * kStage;          // 128 rows x 128 B
 constexpr int kOffR = kOffS + 16384;       // 64 rows x 128 B
@@ -126,7 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
                     const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu,
-                    const int32_t* __restrict__ chunk_off, const float* init, __nv_bfloat16* __restrict__ out,
+                    const int32_t* __restrict__ chunk_off, const float* __restrict__ ws_rn, const float* init,
+                    __nv_bfloat16* __restrict__ out,
                     float* fin, int* __restrict__ err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
                     long long nslots, int norm_qk, int h_base) {
   extern __shared__ unsigned char smem_raw[];
@@ -220,6 +223,11 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const size_t off = ok ? (size_t)(sq.bos + (long long)c * kChunk + tid) * Hv + h : 0;
       cp_async4(st + kOffG + 4 * tid, g + off, ok);
       cp_async4(st + kOffB + 4 * tid, beta + off, ok);
+      if (norm_qk) {  // the chunk's inverse norms, from the preparation kernel
+        const float* rn = ws_rn + ((size_t)(slot0 + c) * Hk + hk) * (2 * kChunk);
+        cp_async4(st + kOffRN + 4 * tid, rn + tid, true);
+        cp_async4(st + kOffRN + 256 + 4 * tid, rn + kChunk + tid, true);
+      }
     }
   };
 
@@ -310,8 +318,8 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const float eC = expf(glast);
     const float b_t = bs[tok];
     // with in-kernel q/k normalisation, this token's inverse norm (k rows for the
-    // R / dU epilogues, q rows for the outputs); computed while phase 1 runs
-    const float rn = norm_qk ? tc::inv_norm(tc::row_sumsq_sw128<DK>(st + kOffKQ, tok + (q4 < 2 ? 0 : 64))) : 1.f;
+    // R / dU epilogues, q rows for the outputs), as the preparation kernel summed it
+    const float rn = norm_qk ? reinterpret_cast<const float*>(st + kOffRN)[tok + (q4 < 2 ? 0 : 64)] : 1.f;
 
     // ---- phase-1 epilogue: R = beta V - beta e X (rows 0..63), keep Y (rows 64..127)
     if (!tc::mbar_wait(&bars[0], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
@@ -451,7 +459,8 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 template <int DK>
 cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                            const int32_t* cu, const int32_t* chunk_off, const void* ws, const float* init,
+                            const int32_t* cu, const int32_t* chunk_off, const void* ws, const float* ws_rn,
+                            const float* init,
                             void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
                             long long nslots, int norm_qk, int h_base, int h_count, cudaStream_t st) {
   const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
@@ -481,7 +490,7 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
   cudaError_t e = set_smem_limit_once<gdn_chain_tc_kernel<DK>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)B * (DV / kDVT), h_count);  // value heads h_base .. h_base + h_count - 1
-  gdn_chain_tc_kernel<DK><<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, init,
+  gdn_chain_tc_kernel<DK><<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, ws_rn, init,
                                                                static_cast<__nv_bfloat16*>(out), fin, err, B, T,
                                                                Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base);
   return cudaGetLastError();
@@ -489,7 +498,8 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
 
 #define GDN_INST_CHAIN_TC(DK)                                                                                \
   template cudaError_t launch_chain_tc<DK>(const void*, const void*, const void*, const float*, const float*, \
-                                           const int32_t*, const int32_t*, const void*, const float*, void*,  \
+                                           const int32_t*, const int32_t*, const void*, const float*,         \
+                                           const float*, void*,                                               \
                                            float*, int*, int, int, int, int, int, int, long long, int, int,   \
                                            int, cudaStream_t);
 GDN_INST_CHAIN_TC(32)

@@ -15,6 +15,10 @@ constexpr int kChunk = 64;  // tokens per chunk
 // ---------------------------------------------------------------------------
 constexpr int kWsTileElems = kChunk * kChunk;           // 4096 bf16
 constexpr size_t kWsPerSlotHead = 2 * kWsTileElems * 2;  // bytes (Tm + PT)
+// After the tiles, per (chunk slot, key head): the inverse L2 norms of the chunk's
+// k rows then q rows (fp32, 64 + 64), written by the preparation kernel when q and k
+// are normalised in-kernel.
+constexpr size_t kWsNormPerSlotKHead = 2 * kChunk * 4;  // bytes
 
 struct SeqChunk {
   long long bos;  // first token of the sequence

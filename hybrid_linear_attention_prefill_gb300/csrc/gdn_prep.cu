@@ -93,8 +93,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                 const float* __restrict__ g, const float* __restrict__ beta,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_off,
-                __nv_bfloat16* __restrict__ ws, int* __restrict__ err, int B, int T, int Hk, int Hv,
-                int nc_dense, int norm_qk, int hk_base) {
+                __nv_bfloat16* __restrict__ ws, float* __restrict__ ws_rn, int* __restrict__ err, int B,
+                int T, int Hk, int Hv, int nc_dense, int norm_qk, int hk_base) {
   using L = PrepSmem<DK>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -203,6 +203,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   if (tid < 2 * kChunk) {
     const float r = norm_qk ? tc::inv_norm(tc::row_sumsq_sw128<DK>(KQ, (tid & 63) + 64 * (tid >> 6))) : 1.f;
     rnk[tid] = r;  // tid 0..63: k rows, 64..127: q rows (rnq = rnk + 64)
+    if (norm_qk) ws_rn[((size_t)slot * Hk + hk) * (2 * kChunk) + tid] = r;  // for the state carry
   }
   if (!tc::mbar_wait(&bar[1], 0, 1u << 24)) atomicOr(err, 4);
   tc::fence_after();
@@ -475,7 +476,7 @@ PFN_cuTensorMapEncodeTiled_v12000 prep_map_encoder() {
 
 template <int DK>
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const float* beta,
-                        const int32_t* cu, const int32_t* chunk_off, void* ws, int* err, int B, int T,
+                        const int32_t* cu, const int32_t* chunk_off, void* ws, float* ws_rn, int* err, int B, int T,
                         int Hk, int Hv, int nslots, int nc_dense, int norm_qk, int hk_base, int hk_count,
                         cudaStream_t st) {
   using L = PrepSmem<DK>;
@@ -497,7 +498,7 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   if (e != cudaSuccess) return e;
   dim3 grid(nslots, hk_count);  // key heads hk_base .. hk_base + hk_count - 1
   gdn_prep_kernel<DK><<<grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
-                                                           static_cast<__nv_bfloat16*>(ws), err, B, T, Hk, Hv,
+                                                           static_cast<__nv_bfloat16*>(ws), ws_rn, err, B, T, Hk, Hv,
                                                            nc_dense, norm_qk, hk_base);
   return cudaGetLastError();
 }
@@ -509,8 +510,8 @@ cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_o
 
 #define GDN_INST_PREP(DK)                                                                                  \
   template cudaError_t launch_prep<DK>(const void*, const void*, const float*, const float*, const int32_t*, \
-                                       const int32_t*, void*, int*, int, int, int, int, int, int, int, int, int,  \
-                                       cudaStream_t);
+                                       const int32_t*, void*, float*, int*, int, int, int, int, int, int, int,  \
+                                       int, int, cudaStream_t);
 GDN_INST_PREP(32)
 GDN_INST_PREP(64)
 GDN_INST_PREP(128)

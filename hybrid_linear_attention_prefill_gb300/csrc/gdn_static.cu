@@ -30,12 +30,12 @@
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, int*, int, int, int, int, int, int, int, int, int, cudaStream_t);
+                        void*, float*, int*, int, int, int, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
-                            const int32_t*, const void*, const float*, void*, float*, int*, int, int, int, int, int,
-                            int, long long, int, int, int, cudaStream_t);
+                            const int32_t*, const void*, const float*, const float*, void*, float*, int*, int, int,
+                            int, int, int, int, long long, int, int, int, cudaStream_t);
 }  // namespace gdn
 
 namespace {
@@ -67,10 +67,12 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   if (ntok == 0 && final_state == nullptr) return GDN_OK;
 
   // scratch layout: [256 B status words][chunk table, B + 1 int32, padded to 256 B][Tm/PT tiles]
+  //                 [inverse q/k norms per (slot, key head)]
   const long long nslots = packed ? (long long)(T + gdn::kChunk - 1) / gdn::kChunk + B
                                   : (long long)B * ((T + gdn::kChunk - 1) / gdn::kChunk);
   const size_t table = round256(sizeof(int32_t) * ((size_t)B + 1));
-  const size_t need = 256 + table + (size_t)nslots * Hv * gdn::kWsPerSlotHead;
+  const size_t need = 256 + table + (size_t)nslots * Hv * gdn::kWsPerSlotHead +
+                      (size_t)nslots * Hk * gdn::kWsNormPerSlotKHead;
   if (need > (size_t)GDN_STATIC_SCRATCH_BYTES || nslots > 0x7fffffffLL) return GDN_ERR_SCRATCH;
 
   int dev = 0;
@@ -93,6 +95,7 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   int* err = static_cast<int*>(base);
   int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + 256);
   void* tiles = static_cast<unsigned char*>(base) + 256 + table;
+  float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   if (packed) {
     e = gdn::launch_chunk_table(cu_seqlens, B, T, chunk_off, st);
@@ -100,16 +103,16 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   }
   if (nslots > 0) {
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, st); break;
     }
     if (e != cudaSuccess) return GDN_ERR_LAUNCH;
   }
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, st); break;
   }
   if (e != cudaSuccess) return GDN_ERR_LAUNCH;
   return GDN_OK;

@@ -211,8 +211,9 @@ void gdn_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end);
  * loading the library holds until the process exits; it calls no allocator.
  *   - Returns GDN_ERR_SCRATCH, before launching anything, when the problem needs
  *     more scratch than that.  gdn_workspace_bytes gives the need: 16 KiB per
- *     (64-token chunk, value head) pair plus a small table, so the array covers up
- *     to 4,095 pairs -- for example one 4,096-token sequence with 32 value heads.
+ *     (64-token chunk, value head) pair, 512 B per (chunk, key head) pair and a
+ *     small table -- for example 32.5 MiB for one 4,096-token sequence with 32
+ *     value heads over 16 key heads.
  *   - All calls on a device share the array and it keeps the last call's contents.
  *     Calls whose GPU work overlaps (other streams, other host threads) race on it:
  *     the caller must order them.

@@ -82,9 +82,10 @@ def test_host_entry_rejects_bad_arguments(lib):
 
 
 def test_workspace_bytes(lib):
-    per = 2 * 64 * 64 * 2
-    assert gdn.gdn_workspace_bytes(1, 4096, 16, 32, 128, 128, 0) == 512 + 64 * 32 * per
-    assert gdn.gdn_workspace_bytes(2, 100, 1, 1, 32, 32, 1) == 512 + (2 + 2) * per
+    per = 2 * 64 * 64 * 2   # Tm + PT per (chunk slot, value head)
+    norms = 2 * 64 * 4      # inverse q/k norms per (chunk slot, key head)
+    assert gdn.gdn_workspace_bytes(1, 4096, 16, 32, 128, 128, 0) == 512 + 64 * 32 * per + 64 * 16 * norms
+    assert gdn.gdn_workspace_bytes(2, 100, 1, 1, 32, 32, 1) == 512 + (2 + 2) * (per + norms)
     assert gdn.gdn_workspace_bytes(1, 10, 2, 3, 128, 128, 0) == 0
 
 
