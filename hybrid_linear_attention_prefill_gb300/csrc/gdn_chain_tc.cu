@@ -123,7 +123,9 @@ __device__ __forceinline__ void sum_parts(uint32_t taddr, int cg, float (&acc)[1
 
 }  // namespace
 
-template <int DK>
+// kNorm: q and k are normalised in-kernel (their inverse norms come from the
+// preparation kernel); a separate instantiation keeps the plain path free of it.
+template <int DK, bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
@@ -131,7 +133,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const int32_t* __restrict__ chunk_off, const float* __restrict__ ws_rn, const float* init,
                     __nv_bfloat16* __restrict__ out,
                     float* fin, int* __restrict__ err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
-                    long long nslots, int norm_qk, int h_base) {
+                    long long nslots, int h_base) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
@@ -223,7 +225,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const size_t off = ok ? (size_t)(sq.bos + (long long)c * kChunk + tid) * Hv + h : 0;
       cp_async4(st + kOffG + 4 * tid, g + off, ok);
       cp_async4(st + kOffB + 4 * tid, beta + off, ok);
-      if (norm_qk) {  // the chunk's inverse norms, from the preparation kernel
+      if (kNorm) {  // the chunk's inverse norms, from the preparation kernel
         const float* rn = ws_rn + ((size_t)(slot0 + c) * Hk + hk) * (2 * kChunk);
         cp_async4(st + kOffRN + 4 * tid, rn + tid, true);
         cp_async4(st + kOffRN + 256 + 4 * tid, rn + kChunk + tid, true);
@@ -319,7 +321,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const float b_t = bs[tok];
     // with in-kernel q/k normalisation, this token's inverse norm (k rows for the
     // R / dU epilogues, q rows for the outputs), as the preparation kernel summed it
-    const float rn = norm_qk ? reinterpret_cast<const float*>(st + kOffRN)[tok + (q4 < 2 ? 0 : 64)] : 1.f;
+    const float rn = kNorm ? reinterpret_cast<const float*>(st + kOffRN)[tok + (q4 < 2 ? 0 : 64)] : 1.f;
 
     // ---- phase-1 epilogue: R = beta V - beta e X (rows 0..63), keep Y (rows 64..127)
     if (!tc::mbar_wait(&bars[0], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
@@ -487,12 +489,14 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
     const cuuint32_t box[2] = {64, 128};
     if (!make_map(&mw, ws, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
   }
-  cudaError_t e = set_smem_limit_once<gdn_chain_tc_kernel<DK>>(kSmemBytes);
+  auto* kernel = norm_qk ? gdn_chain_tc_kernel<DK, true> : gdn_chain_tc_kernel<DK, false>;
+  cudaError_t e = norm_qk ? set_smem_limit_once<gdn_chain_tc_kernel<DK, true>>(kSmemBytes)
+                          : set_smem_limit_once<gdn_chain_tc_kernel<DK, false>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)B * (DV / kDVT), h_count);  // value heads h_base .. h_base + h_count - 1
-  gdn_chain_tc_kernel<DK><<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, ws_rn, init,
-                                                               static_cast<__nv_bfloat16*>(out), fin, err, B, T,
-                                                               Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base);
+  kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, ws_rn, init,
+                                              static_cast<__nv_bfloat16*>(out), fin, err, B, T, Hk, Hv, DV,
+                                              nc_dense, nslots, h_base);
   return cudaGetLastError();
 }
 
