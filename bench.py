@@ -530,7 +530,8 @@ def run_reference_arm(args):
     sample = (f"first {sub.total_tokens} of {inp.total_tokens} tokens, all {inp.Hv} value heads per step, "
               "float64 token loop")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "B": inp.B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv,
