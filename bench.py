@@ -114,7 +114,11 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples (summarised into the JSON line) go to $GDN_BENCH_OUT or the temp directory
+        import tempfile
+
+        out_dir = os.environ.get("GDN_BENCH_OUT") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
