@@ -173,9 +173,10 @@ def to_device(inp, torch, dev):
                 init=None if inp.init is None else t(inp.init))
 
 
-def cpu_baseline_oracle(inp, target_s=8.0):
+def cpu_baseline_oracle(inp, target_s=1.5):
     """Time the float64 oracle as it stands on the host cores on a bounded sample:
-    all value heads of the first `n` tokens of every sequence, n sized to ~target_s."""
+    all value heads of the first `n` tokens of every sequence, n sized to ~target_s of
+    wall time; when the whole workload takes less, it is run again until ~target_s."""
     import oracle
 
     cores = oracle.num_cpus()
@@ -187,12 +188,15 @@ def cpu_baseline_oracle(inp, target_s=8.0):
     dt = max(time.perf_counter() - t0, 1e-4)
     n = int(min(inp.total_tokens, max(n_cal, n_cal * target_s / dt)))
     sub = slice_tokens(inp, n)
-    t0 = time.perf_counter()
-    oracle.prefill_inputs(sub, want_final=True, nthreads=cores)
-    dt = time.perf_counter() - t0
-    return {"value": sub.total_tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    runs, dt = 0, 0.0
+    while runs == 0 or (dt < target_s and runs < 64):
+        t0 = time.perf_counter()
+        oracle.prefill_inputs(sub, want_final=True, nthreads=cores)
+        dt += time.perf_counter() - t0
+        runs += 1
+    return {"value": runs * sub.total_tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"first {sub.total_tokens} of {inp.total_tokens} tokens, all {inp.Hv} value heads, "
-                      f"float64 token loop, {dt:.2f} s wall"}
+                      f"float64 token loop, {runs} run(s), {dt:.2f} s wall"}
 
 
 def slice_tokens(inp, n):
