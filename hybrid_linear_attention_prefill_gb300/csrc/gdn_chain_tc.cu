@@ -18,16 +18,19 @@
 // "Open-Jev-27B-v1.1 native text worker" page, "Validation and optimization
 // scope").
 //
-// Latency, not arithmetic, bounds this loop: on sm_103a an MMA that accumulates
-// into the accumulator of the previous one waits ~200 cycles for it, while
-// independent MMAs issue every ~90 cycles whatever their N (up to 256).  So
+// Latency, not arithmetic, bounds this loop.  On sm_103a one thread issues a
+// tcgen05.mma of M = 64 or 128 and N <= 64 every ~45 cycles, whether or not it
+// accumulates into the previous one's accumulator, and the result is visible
+// ~60 cycles after the last issue; at N = 64 the tensor math itself would take
+// ~37 cycles.  So
 //  * the operand that carries the state in each phase (S, R, diag(d) U) is
 //    split into bf16 hi and lo parts that are stacked along N (N = 64: columns
 //    0..31 hi, 32..63 lo) instead of being issued as two MMAs, keeping the fp32
 //    state accurate to ~2^-16 at no extra MMA;
-//  * each phase splits its K dimension over independent TMEM accumulators (4 in
-//    phase 1, 2 in phases 2 and 3; 64 columns each, 256 allocated) that the
-//    epilogue adds up -- more would cost more in TMEM reads than they save.
+//  * phase 1 splits its K = dk steps over two TMEM accumulators, phases 2 and 3
+//    use one (64 columns each, 128 allocated): each extra accumulator costs the
+//    epilogue another 32-column TMEM read per thread, and measured, two in
+//    phase 1 and one in phases 2-3 is fastest.
 // A ninth warp only issues: the MMAs of each phase (ending with a tcgen05.commit
 // on an mbarrier) and the TMA loads of the next chunk (K, Q, the value slice
 // and the [Tm; PT] tile: 5-6 bulk-tensor copies into the other of two stages).
@@ -55,9 +58,9 @@ namespace {
 constexpr int kDVT = 32;        // state rows per CTA
 constexpr int kThreads = 288;   // 8 epilogue warps + 1 issue warp
 constexpr int kEpiThreads = 256;
-constexpr uint32_t kTmemCols = 256;
-constexpr int kParts = 4;       // independent accumulators in phase 1 (K = dk)
-constexpr int kParts23 = 2;     // and in phases 2 and 3 (K = 64)
+constexpr uint32_t kTmemCols = 128;
+constexpr int kParts = 2;       // accumulators in phase 1 (K = dk)
+constexpr int kParts23 = 1;     // and in phases 2 and 3 (K = 64)
 constexpr uint32_t kMaxPolls = 1u << 24;
 
 // stage layout (bytes)
@@ -260,7 +263,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int ks = 0; ks < DK / 16; ++ks) {
           const uint64_t a = tc::sdesc(st_s + kOffKQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSw128);
           const uint64_t bd = tc::sdesc(sb + kOffS + ks * 2048, 0, 1024, tc::kSw128);
-          tc::mma_bf16(tmem + 64 * (ks & 3), a, bd, kID_KS, ks >= kParts);
+          tc::mma_bf16(tmem + 64 * (ks % kP1), a, bd, kID_KS, ks >= kP1);
         }
         tc::commit(&bars[0]);
         // the other stage was last read by the previous chunk's MMAs, which are done
@@ -276,7 +279,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t a = tc::sdesc(st_s + kOffTP + ks * 32, 16, 1024, tc::kSw128);
           const uint64_t bd = tc::sdesc(sb + kOffR + ks * 2048, 0, 1024, tc::kSw128);
-          tc::mma_bf16(tmem + 64 * (ks & 1), a, bd, kID_KS, ks >= kParts23);
+          tc::mma_bf16(tmem + 64 * (ks % kParts23), a, bd, kID_KS, ks >= kParts23);
         }
         tc::commit(&bars[1]);
       }
@@ -290,7 +293,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t a = tc::sdesc(st_s + kOffKQ + ks * 2048, 16384, 1024, tc::kSw128);
           const uint64_t bd = tc::sdesc(sb + kOffU + ks * 2048, 0, 1024, tc::kSw128);
-          tc::mma_bf16(tmem + 64 * (ks & 1), a, bd, kID_KT, ks >= kParts23);
+          tc::mma_bf16(tmem + 64 * (ks % kParts23), a, bd, kID_KT, ks >= kParts23);
         }
         tc::commit(&bars[2]);
       }
