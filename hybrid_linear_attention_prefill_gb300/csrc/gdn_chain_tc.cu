@@ -32,8 +32,11 @@
 //    epilogue another 32-column TMEM read per thread, and measured, two in
 //    phase 1 and one in phases 2-3 is fastest.
 // A ninth warp only issues: the MMAs of each phase (ending with a tcgen05.commit
-// on an mbarrier) and the TMA loads of the next chunk (K, Q, the value slice
-// and the [Tm; PT] tile: 5-6 bulk-tensor copies into the other of two stages).
+// on an mbarrier) and the TMA loads two chunks ahead (K, Q, the value slice and
+// the [Tm; PT] tile: 5-6 bulk-tensor copies into a ring of three stages).  A
+// chunk's copies take about a microsecond to land under the load of all CTAs,
+// about half a chunk step, so one stage ahead would leave them on the critical
+// path.
 // Epilogue warps w and w + 4 read the same 32 TMEM lanes (rows) and split the
 // 32 state columns between them.  The state S stays in fp32 registers.
 //
@@ -71,13 +74,15 @@ constexpr int kOffG = kOffV + 4096;        // 64 fp32
 constexpr int kOffB = kOffG + 256;         // 64 fp32
 constexpr int kOffRN = kOffB + 256;        // 128 fp32: inverse norms of the k rows, then the q rows
 constexpr int kStage = 54272;              // 53 KB, multiple of 1024
+constexpr int kStages = 3;                 // TMA ring: chunk c + 2 loads during chunk c
 static_assert(kOffRN + 512 <= kStage, "stage layout");
-// B operands after the two stages
-constexpr int kOffS = 2 * kStage;          // 128 rows x 128 B
+// B operands after the stages
+constexpr int kOffS = kStages * kStage;    // 128 rows x 128 B
 constexpr int kOffR = kOffS + 16384;       // 64 rows x 128 B
 constexpr int kOffU = kOffR + 8192;        // 64 rows x 128 B
-constexpr int kOffBar = kOffU + 8192;      // 3 MMA mbarriers, 2 load mbarriers, TMEM base, abort flag
+constexpr int kOffBar = kOffU + 8192;      // 3 MMA mbarriers, 3 load mbarriers, TMEM base, abort flag
 constexpr int kSmemBytes = kOffBar + 64 + 1024;  // + slack for 1024-byte alignment
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 constexpr uint32_t kID_KS = tc::idesc_bf16(128, 2 * kDVT, 0, 1);  // A K-major, B MN-major
 constexpr uint32_t kID_KT = tc::idesc_bf16(128, 2 * kDVT, 1, 1);  // A MN-major, B MN-major
@@ -144,9 +149,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const uint32_t sb = raw_s + pad;  // shared-window address of sm
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);        // [0..2] MMA phases
-  uint64_t* full = bars + 3;                                          // [0..1] stage loaded
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 40);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffBar + 44);
+  uint64_t* full = bars + 3;                                          // [0..2] stage loaded
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 48);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffBar + 52);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 8;
@@ -174,7 +179,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) tc::mbar_init(&bars[i], 1);
+    for (int i = 0; i < 3 + kStages; ++i) tc::mbar_init(&bars[i], 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -185,7 +190,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     tc::prefetch_tensormap(&tm_w);
   }
   if (kKBlocks == 1 && !issuer) {  // phase 3 reads all 128 rows of K^T: the rows d >= 64 stay zero
-    for (int e = tid; e < 2 * 1024; e += kEpiThreads) {
+    for (int e = tid; e < kStages * 1024; e += kEpiThreads) {
       const int stg = e >> 10, w = e & 1023;
       *reinterpret_cast<uint4*>(sm + stg * kStage + kOffKQ + 16384 + w * 16) = make_uint4(0, 0, 0, 0);
     }
@@ -237,7 +242,10 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   };
 
   if (nchunks > 0) {
-    if (issuer && lane == 0) load_tiles(0, 0);
+    if (issuer && lane == 0) {
+      load_tiles(0, 0);
+      if (nchunks > 1) load_tiles(1, 1);
+    }
     load_scalars(0, 0);
   }
   cp_async_commit();
@@ -246,12 +254,12 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   bool aborted = false;
   int c = 0;
   for (; c < nchunks; ++c) {
-    const int stg = c & 1;
+    const int stg = c % kStages;
     const uint32_t par = (uint32_t)(c & 1);
     unsigned char* st = sm + stg * kStage;
     const uint32_t st_s = sb + stg * kStage;
     cp_async_wait<0>();
-    if (!tc::mbar_wait(&full[stg], (uint32_t)((c >> 1) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
+    if (!tc::mbar_wait(&full[stg], (uint32_t)((c / kStages) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
     __syncthreads();
     if (*abort_flag) { aborted = true; break; }
 
@@ -266,8 +274,8 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           tc::mma_bf16(tmem + 64 * (ks % kP1), a, bd, kID_KS, ks >= kP1);
         }
         tc::commit(&bars[0]);
-        // the other stage was last read by the previous chunk's MMAs, which are done
-        if (c + 1 < nchunks) load_tiles(c + 1, stg ^ 1);
+        // stage (c + 2) % 3 was last read by the previous chunk's MMAs, which are done
+        if (c + 2 < nchunks) load_tiles(c + 2, (c + 2) % kStages);
       }
       __syncwarp();
       __syncthreads();  // R written
@@ -302,7 +310,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     }
 
     // ================= epilogue warps =================
-    if (c + 1 < nchunks) load_scalars(c + 1, stg ^ 1);
+    if (c + 1 < nchunks) load_scalars(c + 1, (c + 1) % kStages);
     cp_async_commit();
 
     // per-token scalars: every warp scans the 64 log decays of the chunk
@@ -410,7 +418,8 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // let MMAs and TMA copies still in flight land before the CTA exits (bounded again)
     const uint32_t par = (uint32_t)(c & 1);
     for (int i = 0; i < 3; ++i) (void)tc::mbar_wait(&bars[i], par, 1u << 16);
-    for (int i = 0; i < 2; ++i) (void)tc::mbar_wait(&full[(c + i) & 1], (uint32_t)(((c + i) >> 1) & 1), 1u << 16);
+    for (int i = 0; i < kStages; ++i)
+      (void)tc::mbar_wait(&full[(c + i) % kStages], (uint32_t)(((c + i) / kStages) & 1), 1u << 16);
   }
   tc::fence_before();
   __syncthreads();
