@@ -73,7 +73,7 @@ __device__ __forceinline__ void store_tile(float* D, int ldd, int r0, int n0, co
 template <int DK>
 struct PrepSmem {
   // [union: K,Q tiles (TMA, 128 B swizzle) | A,Tm fp32] [G fp32 x2] [P bf16] [Tm bf16] [merge buffer]
-  // [gamma, beta] [mbarrier]
+  // [inverse norms] [g, beta] [mbarriers]
   static constexpr int kKQBytes = 32768;
   static constexpr int kATBytes = 2 * kChunk * LDF * 4;
   static constexpr int kUnion = kKQBytes > kATBytes ? kKQBytes : kATBytes;
@@ -81,8 +81,7 @@ struct PrepSmem {
   static constexpr int offP = offG + 2 * kChunk * LDF * 4;
   static constexpr int offTb = offP + kChunk * LDB * 2;
   static constexpr int offW = offTb + kChunk * LDB * 2;
-  static constexpr int offGam = offW + 32 * LDW * 4;
-  static constexpr int offRN = offGam + 2 * kChunk * 4;  // inverse norms of k rows, then q rows
+  static constexpr int offRN = offW + 32 * LDW * 4;  // inverse norms of k rows, then q rows
   static constexpr int offGB = offRN + 2 * kChunk * 4;   // [2 buffers][g 64 | beta 64] fp32
   static constexpr int offBar = offGB + 2 * 2 * kChunk * 4;
   static constexpr int bytes = offBar + 32 + 1024;  // 2 mbarriers + TMEM base; + slack for 1024-byte alignment
@@ -106,8 +105,6 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   __nv_bfloat16* Ps = reinterpret_cast<__nv_bfloat16*>(smem + L::offP);
   __nv_bfloat16* Tmb = reinterpret_cast<__nv_bfloat16*>(smem + L::offTb);
   float* Wt = reinterpret_cast<float*>(smem + L::offW);  // [32][LDW]
-  float* gam = reinterpret_cast<float*>(smem + L::offGam);
-  float* bet = gam + kChunk;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::offBar);  // [0] tiles loaded, [1] Grams done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offBar + 16);
   float* gbuf = reinterpret_cast<float*>(smem + L::offGB);
@@ -227,45 +224,47 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     cp_async_wait<0>();
     __syncthreads();
     if (gi + 1 < G) prefetch_gb(gi + 1, (gi + 1) & 1);
-    // ---- gamma = inclusive cumsum of g in the chunk -------------------------
-    if (warp == 0) {
-      const float* gb = gbuf + (gi & 1) * 2 * kChunk;
-      float g0 = gb[lane], g1 = gb[lane + 32];
-      const float b0 = gb[kChunk + lane], b1 = gb[kChunk + lane + 32];
+    // ---- gamma = inclusive cumsum of g in the chunk, in log2 units -------------------
+    // Every warp scans the 64 values in registers (lane l holds tokens l and l + 32), so
+    // no warp waits for another; the A/P build below takes its entries by shuffle.
+    const float* gb = gbuf + (gi & 1) * 2 * kChunk;  // [g 64 | beta 64]
+    float gl0 = gb[lane], gl1 = gb[lane + 32];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u0 = __shfl_up_sync(0xffffffffu, g0, o);
-        const float u1 = __shfl_up_sync(0xffffffffu, g1, o);
-        if (lane >= o) { g0 += u0; g1 += u1; }
-      }
-      g1 += __shfl_sync(0xffffffffu, g0, 31);
-      gam[lane] = g0 * 1.4426950408889634f;  // log2(e)
-      gam[lane + 32] = g1 * 1.4426950408889634f;
-      bet[lane] = b0;
-      bet[lane + 32] = b1;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u0 = __shfl_up_sync(0xffffffffu, gl0, o);
+      const float u1 = __shfl_up_sync(0xffffffffu, gl1, o);
+      if (lane >= o) { gl0 += u0; gl1 += u1; }
     }
-    __syncthreads();
+    gl1 += __shfl_sync(0xffffffffu, gl0, 31);
+    gl0 *= 1.4426950408889634f;  // log2(e)
+    gl1 *= 1.4426950408889634f;
 
     // ---- A (fp32) and P (bf16), 8 columns at a time, lower triangle only ----------
     // Gamma[t][i] = 2^(gamma2_t - gamma2_i) with gamma2 = gamma log2(e): the exponent
     // is never positive for i <= t.  A thread keeps one 8-column block (the CTA size is
     // a multiple of 8), so its gamma and 1/||k|| columns are loaded once.
-    static_assert(kPrepThreads % 8 == 0, "column block fixed per thread");
+    static_assert(kPrepThreads == 256, "two (row, column block) items per thread, rows tid / 8 and + 32");
     const int c8 = (tid & 7) * 8;
     float gcol[8], rcol[8];
     {
-      const float4 g0 = *reinterpret_cast<const float4*>(gam + c8), g1 = *reinterpret_cast<const float4*>(gam + c8 + 4);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {  // gamma of columns c8 .. c8 + 7 (tokens < 32 in gl0, the rest in gl1)
+        const float lo = __shfl_sync(0xffffffffu, gl0, (c8 + u) & 31);
+        const float hi = __shfl_sync(0xffffffffu, gl1, (c8 + u) & 31);
+        gcol[u] = c8 < 32 ? lo : hi;
+      }
       const float4 r0 = *reinterpret_cast<const float4*>(rnk + c8), r1 = *reinterpret_cast<const float4*>(rnk + c8 + 4);
-      gcol[0] = g0.x; gcol[1] = g0.y; gcol[2] = g0.z; gcol[3] = g0.w;
-      gcol[4] = g1.x; gcol[5] = g1.y; gcol[6] = g1.z; gcol[7] = g1.w;
       rcol[0] = r0.x; rcol[1] = r0.y; rcol[2] = r0.z; rcol[3] = r0.w;
       rcol[4] = r1.x; rcol[5] = r1.y; rcol[6] = r1.z; rcol[7] = r1.w;
     }
+    // gamma of this thread's two rows, tid / 8 and tid / 8 + 32 (lane (tid / 8) % 32 of this warp)
+    const float grow0 = __shfl_sync(0xffffffffu, gl0, (tid >> 3) & 31);
+    const float grow1 = __shfl_sync(0xffffffffu, gl1, (tid >> 3) & 31);
     for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
       const int t = e >> 3;
       float av[8], pv[8];
       if (c8 <= t) {
-        const float gt = gam[t], bt = bet[t] * rnk[t], qt = rnq[t];
+        const float gt = t < 32 ? grow0 : grow1, bt = gb[kChunk + t] * rnk[t], qt = rnq[t];
         const float4 k0 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8);
         const float4 k1 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8 + 4);
         const float4 q0 = *reinterpret_cast<const float4*>(Gs + kChunk * LDF + t * LDF + c8);
