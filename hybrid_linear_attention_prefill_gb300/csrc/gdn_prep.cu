@@ -113,6 +113,10 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = blockIdx.x, hk = hk_base + (int)blockIdx.y;
+  if (tid == 0) {  // the copies below are this CTA's first work; fetch their descriptors now
+    tc::prefetch_tensormap(&tm_k);
+    tc::prefetch_tensormap(&tm_q);
+  }
 
   // ---- which sequence and chunk this slot is ---------------------------------
   int b, c;
@@ -150,11 +154,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   // ---- TMEM for the Grams; the K and Q tiles by TMA (tokens past the end are zero)
   constexpr int kKBlocks = DK > 64 ? 2 : 1;
   constexpr uint32_t kGramCols = 64;
-  if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, kGramCols);
-    tc::tmem_relinquish();
-  }
-  if (tid == 0) {
+  if (tid == 0) {  // the copies first: the Grams wait for them
     tc::mbar_init(&bar[0], 1);
     tc::mbar_init(&bar[1], 1);
     tc::fence_mbar_init();
@@ -164,6 +164,11 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       tc::tma_load_3d(KQ + db * 16384, &tm_k, 64 * db, hk, (int)t0, &bar[0]);
       tc::tma_load_3d(KQ + db * 16384 + 8192, &tm_q, 64 * db, hk, (int)t0, &bar[0]);
     }
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tc::tmem_alloc(tmem_slot, kGramCols);
+    tc::tmem_relinquish();
   }
   tc::fence_before();
   __syncthreads();
