@@ -138,20 +138,22 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const long long t0 = sq.bos + (long long)c * kChunk;
   const int n = min(kChunk, sq.len - c * kChunk);
 
-  // g and beta of one value head into buffer `buf` (zeros past the chunk's tokens)
+  // g and beta of one value head into buffer `buf` (zeros past the chunk's tokens), by
+  // warps 2 and 3, so that the start-up work of warps 0 and 1 (copies, TMEM) runs beside it
   const int G = Hv / Hk;
   auto prefetch_gb = [&](int gi, int buf) {
-    if (tid < kChunk) {
-      const bool ok = tid < n;
-      const size_t off = ok ? (size_t)(t0 + tid) * Hv + hk * G + gi : 0;
-      cp_async4(gbuf + buf * 2 * kChunk + tid, g + off, ok);
-      cp_async4(gbuf + buf * 2 * kChunk + kChunk + tid, beta + off, ok);
+    const int lt = tid - 64;
+    if (lt >= 0 && lt < kChunk) {
+      const bool ok = lt < n;
+      const size_t off = ok ? (size_t)(t0 + lt) * Hv + hk * G + gi : 0;
+      cp_async4(gbuf + buf * 2 * kChunk + lt, g + off, ok);
+      cp_async4(gbuf + buf * 2 * kChunk + kChunk + lt, beta + off, ok);
     }
     cp_async_commit();
   };
   prefetch_gb(0, 0);
 
-  // ---- TMEM for the Grams; the K and Q tiles by TMA (tokens past the end are zero)
+  // ---- the K and Q tiles by TMA (tokens past the end are zero); TMEM for the Grams
   constexpr int kKBlocks = DK > 64 ? 2 : 1;
   constexpr uint32_t kGramCols = 64;
   if (tid == 0) {  // the copies first: the Grams wait for them
@@ -165,8 +167,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       tc::tma_load_3d(KQ + db * 16384 + 8192, &tm_q, 64 * db, hk, (int)t0, &bar[0]);
     }
   }
-  if (warp == 0) {
-    __syncwarp();
+  if (warp == 1) {  // beside thread 0's copies
     tc::tmem_alloc(tmem_slot, kGramCols);
     tc::tmem_relinquish();
   }
@@ -416,7 +417,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     __syncthreads();
   }
-  if (warp == 0) tc::tmem_dealloc(tmem, kGramCols);
+  if (warp == 1) tc::tmem_dealloc(tmem, kGramCols);
 }
 
 // Prefix sums of chunk counts for packed sequences: chunk_off[b] = sum over
