@@ -11,16 +11,17 @@
 
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
+#include <climits>
 
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, float*, int*, int, int, int, int, int, int, int, int, int, cudaStream_t);
+                        void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
                             const int32_t*, const void*, const float*, const float*, void*, float*, int*, int, int,
-                            int, int, int, int, long long, int, int, int, cudaStream_t);
+                            int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int32_t*, int, int, int, int, int, int, int,
                              cudaStream_t);
@@ -46,13 +47,15 @@ struct DevBuffers {
   cudaStream_t aux = nullptr;  // second stream for pass A's transition run
   cudaEvent_t fork = nullptr, join = nullptr;
   int sms = 0;
-  // gdn_prefill_host's copy / compute pipeline over head groups
+  // gdn_prefill_host's copy / compute pipeline over head groups or token windows
   bool pipe_ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr, comp[3] = {nullptr, nullptr, nullptr};
-  cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[4] = {}, ev_done[4] = {};
+  cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[8] = {}, ev_prep[8] = {}, ev_done[8] = {};
 };
 
-constexpr int kMaxHostGroups = 4;
+constexpr int kMaxHostGroups = 4;   // head groups (packed batches)
+constexpr int kMaxHostWindows = 8;      // token windows (dense batches)
+constexpr int kHostWindowChunks = 16;   // chunks per window, about (measured best over 2..16 windows)
 
 std::mutex g_mu;
 DevBuffers g_dev[kMaxDevices];
@@ -207,7 +210,7 @@ cudaError_t chain(const void* q, const void* k, const void* v, const float* g, c
                   const float* init, void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV,
                   int nc_dense, long long nslots, int norm_qk, cudaStream_t st) {
   return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv,
-                                  DV, nc_dense, nslots, norm_qk, 0, Hv, st);
+                                  DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, st);
 }
 
 cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -226,7 +229,10 @@ cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const 
 int launch_all(const void* q, const void* k, const void* v, const float* g, const float* beta,
                const int32_t* cu, const float* init, void* out, float* fin, int B, int T, int Hk, int Hv,
                int dk, int dv, cudaStream_t st, void* ws, int norm_qk = 0, const ScanPlan* plan = nullptr,
-               int h0 = 0, int h1 = -1, bool table = true) {
+               int h0 = 0, int h1 = -1, bool table = true, int c0 = 0, int c1 = -1, int phases = 3) {
+  // [h0, h1): value heads; [c0, c1): the window of each dense sequence's chunks (-1: all).
+  // A window's launches carry the state from `init` to `fin` over its chunks only.
+  // phases: bit 0 the preparation kernel (and the packed chunk table), bit 1 the state carry.
   if (h1 < 0) h1 = Hv;
   const int G = Hv / Hk;
   const int hk0 = h0 / G, nhk = (h1 - h0) / G;
@@ -236,26 +242,31 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   void* tiles = static_cast<unsigned char*>(ws) + 256 + align_up(sizeof(int32_t) * ((size_t)B + 1), 256);
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   const long long nslots = num_slots(B, T, packed);
+  if (c1 < 0) c1 = nc_dense;
+  const bool whole = c0 == 0 && c1 == nc_dense;
+  if (!packed && (c0 < 0 || c1 > nc_dense || c0 >= c1) && nc_dense > 0) return GDN_ERR_ARG;
+  const int cc0 = packed ? 0 : c0, cc1 = packed ? INT_MAX : c1;  // the chain's window
   float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
   cudaError_t e = cudaSuccess;
-  if (packed && table) {
+  if (packed && table && (phases & 1)) {
     e = gdn::launch_chunk_table(cu, B, T, chunk_off, st);
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
   cudaEvent_t ev[3] = {t_phase_ev[0], t_phase_ev[1], t_phase_ev[2]};
   t_phase_ev[0] = t_phase_ev[1] = t_phase_ev[2] = nullptr;
   if (ev[0] != nullptr && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
-  if (nslots > 0) {
-    if (nslots > 0x7fffffffLL) return GDN_ERR_ARG;
+  if (nslots > 0x7fffffffLL) return GDN_ERR_ARG;
+  if (nslots > 0 && (phases & 1)) {
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, st); break;
     }
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
   if (ev[1] != nullptr && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
-  if (plan != nullptr && plan->P > 1 && !packed && nslots > 0 && h0 == 0 && h1 == Hv) {
+  if (!(phases & 2)) return GDN_OK;
+  if (plan != nullptr && plan->P > 1 && !packed && nslots > 0 && h0 == 0 && h1 == Hv && whole) {
     // ---- two-level scan over P segments per sequence (see gdn_scan.cu) ----------------
     const int P = plan->P, BP = B * P;
     const int cps = (nc_dense + P - 1) / P;  // chunks per segment
@@ -313,9 +324,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     return GDN_OK;
   }
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
   }
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
@@ -494,7 +505,9 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
   const size_t ncu = cu_seqlens ? sizeof(int32_t) * ((size_t)B + 1) : 0;
   const size_t ns = (size_t)B * Hv * dv * dk * 4;
   size_t off[9], total = 0;
-  const size_t sz[9] = {nq, nq, nv, ng, ng, ncu, init_state ? ns : 0, nv, final_state ? ns : 0};
+  // the state slot also carries the state between token windows of a dense batch
+  const size_t sz[9] = {nq, nq, nv, ng, ng, ncu, init_state ? ns : 0, nv,
+                        (final_state != nullptr || cu_seqlens == nullptr) ? ns : 0};
   for (int i = 0; i < 9; ++i) {
     off[i] = total;
     total += align_up(sz[i], 256);
@@ -508,11 +521,15 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
   ScanPlan plan;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   DevBuffers* dp = nullptr;
-  // Head groups: the copies of group i + 1 overlap the kernels of group i (each group on
-  // its own stream, so the latency-bound state carries of all groups run side by side)
-  // and the copy-out of earlier groups.  Whole key heads per group; one group for small
-  // problems or with the two-level scan.
-  int ngroups = 1;
+  // Dense batches: token windows of whole chunks.  The copies of window i + 1 overlap the
+  // kernels of window i and the copy-out of earlier windows; each window's state carry
+  // starts from the state the previous one left, so the tail after the last copy-in is
+  // one window's kernels and copy-out.  Packed batches: head groups, whose copies of group
+  // i + 1 overlap the kernels of group i (each group on its own stream, so the
+  // latency-bound state carries of all groups run side by side).  Whole key heads per
+  // group.  One piece for small problems or with the two-level scan.
+  int ngroups = 1, nwin = 1;
+  const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevBuffers& d = g_dev[dev];
@@ -525,15 +542,21 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
     ws = d.ws;
     rc = prepare_scan(dev, B, T, Hv, dk, dv, cu_seqlens != nullptr, 0u, st, plan);
     if (rc != GDN_OK) return rc;
-    if (plan.P <= 1 && nq + nv >= ((size_t)8 << 20)) ngroups = std::min(kMaxHostGroups, Hk);
-    if (ngroups > 1 && !d.pipe_ready) {
+    if (plan.P <= 1 && nq + nv >= ((size_t)8 << 20)) {
+      if (cu_seqlens == nullptr)
+        nwin = nc_dense < 2 ? 1 : std::min(kMaxHostWindows, std::max(2, nc_dense / kHostWindowChunks));
+      else
+        ngroups = std::min(kMaxHostGroups, Hk);
+    }
+    if ((ngroups > 1 || nwin > 1) && !d.pipe_ready) {
       e = cudaStreamCreateWithFlags(&d.h2d, cudaStreamNonBlocking);
       if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.d2h, cudaStreamNonBlocking);
       for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&d.comp[i], cudaStreamNonBlocking);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_start, cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_end, cudaEventDisableTiming);
-      for (int i = 0; i < kMaxHostGroups && e == cudaSuccess; ++i) {
+      for (int i = 0; i < kMaxHostWindows && e == cudaSuccess; ++i) {
         e = cudaEventCreateWithFlags(&d.ev_in[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_prep[i], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_done[i], cudaEventDisableTiming);
       }
       if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
@@ -542,7 +565,7 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
   }
   auto P = [&](int i) -> unsigned char* { return sz[i] ? base + off[i] : nullptr; };
   const void* src[7] = {q, k, v, g, beta, cu_seqlens, init_state};
-  if (ngroups <= 1) {
+  if (ngroups <= 1 && nwin <= 1) {
     for (int i = 0; i < 7; ++i) {
       if (sz[i] == 0 || src[i] == nullptr) continue;
       e = cudaMemcpyAsync(base + off[i], src[i], sz[i], cudaMemcpyHostToDevice, st);
@@ -566,10 +589,70 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
     return GDN_OK;
   }
 
-  // ---- pipelined over head groups --------------------------------------------------
   DevBuffers& d = *dp;
-  const int G = Hv / Hk;
   auto check = [&](cudaError_t x) { return x == cudaSuccess ? GDN_OK : set_cuda_error(x, GDN_ERR_LAUNCH); };
+  if (nwin > 1) {
+    // ---- dense: pipelined over token windows ------------------------------------------
+    // tokens [ta, tb) of every sequence: B rows of (tb - ta) * row bytes, T * row bytes apart
+    auto rows = [&](unsigned char* dst, const unsigned char* src_, size_t row, int ta, int tb, cudaMemcpyKind kind,
+                    cudaStream_t s_) {
+      return cudaMemcpy2DAsync(dst + (size_t)ta * row, (size_t)T * row, src_ + (size_t)ta * row, (size_t)T * row,
+                               (size_t)(tb - ta) * row, B, kind, s_);
+    };
+    const size_t rq = (size_t)Hk * dk * 2, rv = (size_t)Hv * dv * 2, rg = (size_t)Hv * 4;
+    const size_t rowb[5] = {rq, rq, rv, rg, rg};
+    float* state = reinterpret_cast<float*>(P(8));
+    cudaStream_t ps = d.comp[0];  // the preparation kernels; the state carries stay on `stream`
+    if ((rc = check(cudaEventRecord(d.ev_start, st))) != GDN_OK ||
+        (rc = check(cudaStreamWaitEvent(d.h2d, d.ev_start, 0))) != GDN_OK)
+      return rc;
+    if (init_state != nullptr &&
+        (rc = check(cudaMemcpyAsync(P(6), init_state, ns, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK)
+      return rc;
+    // g and beta whole, first (small)
+    if ((rc = check(cudaMemcpyAsync(P(3), g, ng, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK ||
+        (rc = check(cudaMemcpyAsync(P(4), beta, ng, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK)
+      return rc;
+    for (int i = 0; i < nwin; ++i) {
+      const int c0 = (int)((long long)nc_dense * i / nwin), c1 = (int)((long long)nc_dense * (i + 1) / nwin);
+      const int ta = c0 * gdn::kChunk, tb = std::min(c1 * gdn::kChunk, T);
+      for (int a = 0; a < 3; ++a)
+        if ((rc = check(rows(base + off[a], static_cast<const unsigned char*>(src[a]), rowb[a], ta, tb,
+                             cudaMemcpyHostToDevice, d.h2d))) != GDN_OK)
+          return rc;
+      if ((rc = check(cudaEventRecord(d.ev_in[i], d.h2d))) != GDN_OK ||
+          (rc = check(cudaStreamWaitEvent(ps, d.ev_in[i], 0))) != GDN_OK)
+        return rc;
+      rc = launch_all(P(0), P(1), P(2), reinterpret_cast<const float*>(P(3)), reinterpret_cast<const float*>(P(4)),
+                      nullptr, nullptr, P(7), state, B, T, Hk, Hv, dk, dv, ps, ws, 0, nullptr, 0, -1, false, c0, c1,
+                      1);
+      if (rc != GDN_OK) return rc;
+      if ((rc = check(cudaEventRecord(d.ev_prep[i], ps))) != GDN_OK ||
+          (rc = check(cudaStreamWaitEvent(st, d.ev_prep[i], 0))) != GDN_OK)
+        return rc;
+      const float* win_init = i == 0 ? (init_state ? reinterpret_cast<const float*>(P(6)) : nullptr) : state;
+      rc = launch_all(P(0), P(1), P(2), reinterpret_cast<const float*>(P(3)), reinterpret_cast<const float*>(P(4)),
+                      nullptr, win_init, P(7), state, B, T, Hk, Hv, dk, dv, st, ws, 0, nullptr, 0, -1, false, c0, c1,
+                      2);
+      if (rc != GDN_OK) return rc;
+      if ((rc = check(cudaEventRecord(d.ev_done[i], st))) != GDN_OK ||
+          (rc = check(cudaStreamWaitEvent(d.d2h, d.ev_done[i], 0))) != GDN_OK ||
+          (rc = check(rows(static_cast<unsigned char*>(out), P(7), rv, ta, tb, cudaMemcpyDeviceToHost, d.d2h))) !=
+              GDN_OK)
+        return rc;
+    }
+    if (final_state != nullptr &&
+        (rc = check(cudaMemcpyAsync(final_state, state, ns, cudaMemcpyDeviceToHost, d.d2h))) != GDN_OK)
+      return rc;
+    if ((rc = check(cudaEventRecord(d.ev_end, d.d2h))) != GDN_OK ||
+        (rc = check(cudaStreamWaitEvent(st, d.ev_end, 0))) != GDN_OK ||
+        (rc = check(cudaStreamSynchronize(st))) != GDN_OK)
+      return rc;
+    return GDN_OK;
+  }
+
+  // ---- packed: pipelined over head groups ---------------------------------------------
+  const int G = Hv / Hk;
   auto h2d_cols = [&](int i, size_t col0, size_t width, size_t pitch, size_t rows) {  // column band of a row-major array
     return cudaMemcpy2DAsync(base + off[i] + col0, pitch, static_cast<const unsigned char*>(src[i]) + col0, pitch,
                              width, rows, cudaMemcpyHostToDevice, d.h2d);
@@ -688,8 +771,9 @@ void gdn_release_workspace(void) {
     for (cudaStream_t c : d.comp) cudaStreamDestroy(c);
     cudaEventDestroy(d.ev_start);
     cudaEventDestroy(d.ev_end);
-    for (int i = 0; i < kMaxHostGroups; ++i) {
+    for (int i = 0; i < kMaxHostWindows; ++i) {
       cudaEventDestroy(d.ev_in[i]);
+      cudaEventDestroy(d.ev_prep[i]);
       cudaEventDestroy(d.ev_done[i]);
     }
   }

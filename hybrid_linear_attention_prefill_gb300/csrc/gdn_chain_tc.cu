@@ -141,7 +141,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const int32_t* __restrict__ chunk_off, const float* __restrict__ ws_rn, const float* init,
                     __nv_bfloat16* __restrict__ out,
                     float* fin, int* __restrict__ err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
-                    long long nslots, int h_base) {
+                    long long nslots, int h_base, int c_begin, int c_end) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
@@ -172,6 +172,11 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int slot0 = cu == nullptr ? b * nc_dense : chunk_off[b];
   int nchunks = (sq.len + kChunk - 1) / kChunk;
   if ((long long)slot0 + nchunks > nslots) nchunks = slot0 < nslots ? (int)(nslots - slot0) : 0;
+  // this launch walks chunks c0 .. c1 - 1 of the sequence, from `init` (the state before
+  // chunk c0) to `fin` (the state after chunk c1 - 1): the whole sequence, or a window of
+  // it whose neighbours run as other launches in order
+  const int c0 = c_begin < nchunks ? c_begin : nchunks;
+  const int c1 = c_end < nchunks ? c_end : nchunks;
 
   // ---- set-up: TMEM, barriers, zero d-block 1 when dk <= 64 --------------------
   if (warp == 0) {
@@ -241,25 +246,26 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     }
   };
 
-  if (nchunks > 0) {
+  if (c1 > c0) {
     if (issuer && lane == 0) {
-      load_tiles(0, 0);
-      if (nchunks > 1) load_tiles(1, 1);
+      load_tiles(c0, 0);
+      if (c1 > c0 + 1) load_tiles(c0 + 1, 1);
     }
-    load_scalars(0, 0);
+    load_scalars(c0, 0);
   }
   cp_async_commit();
 
   const int tok = 32 * (q4 & 1) + lane;  // this thread's token in phases 1-2
   bool aborted = false;
-  int c = 0;
-  for (; c < nchunks; ++c) {
-    const int stg = c % kStages;
-    const uint32_t par = (uint32_t)(c & 1);
+  int c = c0;
+  for (; c < c1; ++c) {
+    const int ci = c - c0;  // position in this launch: stage and barrier phases
+    const int stg = ci % kStages;
+    const uint32_t par = (uint32_t)(ci & 1);
     unsigned char* st = sm + stg * kStage;
     const uint32_t st_s = sb + stg * kStage;
     cp_async_wait<0>();
-    if (!tc::mbar_wait(&full[stg], (uint32_t)((c / kStages) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
+    if (!tc::mbar_wait(&full[stg], (uint32_t)((ci / kStages) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
     __syncthreads();
     if (*abort_flag) { aborted = true; break; }
 
@@ -274,8 +280,8 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           tc::mma_bf16(tmem + 64 * (ks % kP1), a, bd, kID_KS, ks >= kP1);
         }
         tc::commit(&bars[0]);
-        // stage (c + 2) % 3 was last read by the previous chunk's MMAs, which are done
-        if (c + 2 < nchunks) load_tiles(c + 2, (c + 2) % kStages);
+        // stage (ci + 2) % 3 was last read by the previous chunk's MMAs, which are done
+        if (c + 2 < c1) load_tiles(c + 2, (ci + 2) % kStages);
       }
       __syncwarp();
       __syncthreads();  // R written
@@ -310,7 +316,7 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     }
 
     // ================= epilogue warps =================
-    if (c + 1 < nchunks) load_scalars(c + 1, (c + 1) % kStages);
+    if (c + 1 < c1) load_scalars(c + 1, (ci + 1) % kStages);
     cp_async_commit();
 
     // per-token scalars: every warp scans the 64 log decays of the chunk
@@ -416,10 +422,11 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   }
   if (aborted && issuer && lane == 0) {
     // let MMAs and TMA copies still in flight land before the CTA exits (bounded again)
-    const uint32_t par = (uint32_t)(c & 1);
+    const int ci = c - c0;
+    const uint32_t par = (uint32_t)(ci & 1);
     for (int i = 0; i < 3; ++i) (void)tc::mbar_wait(&bars[i], par, 1u << 16);
     for (int i = 0; i < kStages; ++i)
-      (void)tc::mbar_wait(&full[(c + i) % kStages], (uint32_t)(((c + i) / kStages) & 1), 1u << 16);
+      (void)tc::mbar_wait(&full[(ci + i) % kStages], (uint32_t)(((ci + i) / kStages) & 1), 1u << 16);
   }
   tc::fence_before();
   __syncthreads();
@@ -476,7 +483,8 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
                             const int32_t* cu, const int32_t* chunk_off, const void* ws, const float* ws_rn,
                             const float* init,
                             void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
-                            long long nslots, int norm_qk, int h_base, int h_count, cudaStream_t st) {
+                            long long nslots, int norm_qk, int h_base, int h_count, int c_begin, int c_end,
+                            cudaStream_t st) {
   const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
   const cuuint64_t tt = (cuuint64_t)(ttot > 0 ? ttot : 1);
   CUtensorMap mk, mq, mv, mw;
@@ -508,7 +516,7 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
   dim3 grid((unsigned)B * (DV / kDVT), h_count);  // value heads h_base .. h_base + h_count - 1
   kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, ws_rn, init,
                                               static_cast<__nv_bfloat16*>(out), fin, err, B, T, Hk, Hv, DV,
-                                              nc_dense, nslots, h_base);
+                                              nc_dense, nslots, h_base, c_begin, c_end);
   return cudaGetLastError();
 }
 
@@ -517,7 +525,7 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
                                            const int32_t*, const int32_t*, const void*, const float*,         \
                                            const float*, void*,                                               \
                                            float*, int*, int, int, int, int, int, int, long long, int, int,   \
-                                           int, cudaStream_t);
+                                           int, int, int, cudaStream_t);
 GDN_INST_CHAIN_TC(32)
 GDN_INST_CHAIN_TC(64)
 GDN_INST_CHAIN_TC(128)

@@ -93,7 +93,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 const float* __restrict__ g, const float* __restrict__ beta,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_off,
                 __nv_bfloat16* __restrict__ ws, float* __restrict__ ws_rn, int* __restrict__ err, int B,
-                int T, int Hk, int Hv, int nc_dense, int norm_qk, int hk_base) {
+                int T, int Hk, int Hv, int nc_dense, int norm_qk, int hk_base, int c_begin, int c_count) {
   using L = PrepSmem<DK>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -112,7 +112,11 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   float* rnq = rnk + kChunk;                                // 1/||q_t||
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slot = blockIdx.x, hk = hk_base + (int)blockIdx.y;
+  // dense batches: CTA x covers chunk c_begin + x % c_count of sequence x / c_count (a window of
+  // each sequence's chunks; the whole sequence when c_begin = 0, c_count = nc_dense)
+  const int slot = cu == nullptr ? (int)(blockIdx.x / c_count) * nc_dense + c_begin + (int)(blockIdx.x % c_count)
+                                 : (int)blockIdx.x;
+  const int hk = hk_base + (int)blockIdx.y;
   if (tid == 0) {  // the copies below are this CTA's first work; fetch their descriptors now
     tc::prefetch_tensormap(&tm_k);
     tc::prefetch_tensormap(&tm_q);
@@ -483,7 +487,7 @@ template <int DK>
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const float* beta,
                         const int32_t* cu, const int32_t* chunk_off, void* ws, float* ws_rn, int* err, int B, int T,
                         int Hk, int Hv, int nslots, int nc_dense, int norm_qk, int hk_base, int hk_count,
-                        cudaStream_t st) {
+                        int c_begin, int c_count, cudaStream_t st) {
   using L = PrepSmem<DK>;
   PFN_cuTensorMapEncodeTiled_v12000 enc = prep_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -501,10 +505,12 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_limit_once<gdn_prep_kernel<DK>>(L::bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(nslots, hk_count);  // key heads hk_base .. hk_base + hk_count - 1
+  if (cu == nullptr && (c_begin < 0 || c_count <= 0 || c_begin + c_count > nc_dense)) return cudaErrorInvalidValue;
+  // key heads hk_base .. hk_base + hk_count - 1; dense: B sequences x c_count chunks
+  dim3 grid(cu == nullptr ? (unsigned)B * (unsigned)c_count : (unsigned)nslots, hk_count);
   gdn_prep_kernel<DK><<<grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
                                                            static_cast<__nv_bfloat16*>(ws), ws_rn, err, B, T, Hk, Hv,
-                                                           nc_dense, norm_qk, hk_base);
+                                                           nc_dense, norm_qk, hk_base, c_begin, c_count);
   return cudaGetLastError();
 }
 
@@ -516,7 +522,7 @@ cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_o
 #define GDN_INST_PREP(DK)                                                                                  \
   template cudaError_t launch_prep<DK>(const void*, const void*, const float*, const float*, const int32_t*, \
                                        const int32_t*, void*, float*, int*, int, int, int, int, int, int, int,  \
-                                       int, int, cudaStream_t);
+                                       int, int, int, int, cudaStream_t);
 GDN_INST_PREP(32)
 GDN_INST_PREP(64)
 GDN_INST_PREP(128)

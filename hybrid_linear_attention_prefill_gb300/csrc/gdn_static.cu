@@ -26,16 +26,17 @@
 
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
+#include <climits>
 
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, float*, int*, int, int, int, int, int, int, int, int, int, cudaStream_t);
+                        void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
                             const int32_t*, const void*, const float*, const float*, void*, float*, int*, int, int,
-                            int, int, int, int, long long, int, int, int, cudaStream_t);
+                            int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
 }  // namespace gdn
 
 namespace {
@@ -103,16 +104,16 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   }
   if (nslots > 0) {
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, st); break;
     }
     if (e != cudaSuccess) return GDN_ERR_LAUNCH;
   }
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
   }
   if (e != cudaSuccess) return GDN_ERR_LAUNCH;
   return GDN_OK;

@@ -117,10 +117,15 @@ int gdn_prefill(const void *q, const void *k, const void *v,
  * gdn_prefill on `stream`, copies out and final_state back and synchronises
  * `stream` before returning.  Page-locked host buffers give the fastest copies.
  * cu_seqlens, init_state and final_state may be NULL as above.  For problems of
- * 8 MB or more (q, k and v together) the work is split into up to four groups of
- * whole key heads: the copies of one group overlap the kernels of the previous
- * one and the copy-back of earlier ones, on library-owned streams that are joined
- * back into `stream`; the results are bit for bit those of gdn_prefill.
+ * 8 MB or more (q, k and v together) the copies overlap the kernels, on
+ * library-owned streams that are joined back into `stream`:
+ *   - equal-length batches: 2 to 8 windows of whole 64-token chunks (about 16
+ *     chunks each).  The copies of one window overlap the kernels of the previous
+ *     one and the copy-back of earlier ones; each window's state carry starts from
+ *     the state the previous window left (kept on the device in fp32);
+ *   - packed batches: up to four groups of whole key heads, whose state carries
+ *     run side by side.
+ * Either way the results are bit for bit those of gdn_prefill.
  */
 int gdn_prefill_host(const void *q, const void *k, const void *v,
                      const float *g, const float *beta,

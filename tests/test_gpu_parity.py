@@ -219,13 +219,15 @@ def test_host_entry_matches_device_entry():
 
 
 @pytest.mark.parametrize("case", [
-    dict(B=1, T=4096, Hk=4, Hv=8, dk=128, dv=128, init_std=0.1),            # 4 head groups, dense
-    dict(lengths=[1500, 0, 2600, 77], Hk=3, Hv=6, dk=128, dv=64, init_std=0.1),  # 3 groups, packed
-    dict(B=2, T=3000, Hk=8, Hv=8, dk=64, dv=128),                             # no initial state
+    dict(B=1, T=4096, Hk=4, Hv=8, dk=128, dv=128, init_std=0.1),            # dense: 8 token windows
+    dict(lengths=[1500, 0, 2600, 77], Hk=3, Hv=6, dk=128, dv=64, init_std=0.1),  # packed: 3 head groups
+    dict(B=2, T=3000, Hk=8, Hv=8, dk=64, dv=128),                             # 2 sequences, ragged last chunk
+    dict(B=1, T=4096, Hk=8, Hv=16, dk=32, dv=32, init_std=0.1),              # small head dims
 ])
-def test_host_entry_pipelined_over_head_groups(case):
-    """Large enough for gdn_prefill_host to overlap its copies with the kernels of head
-    groups on separate streams: bitwise the device entry's results, pinned or pageable."""
+def test_host_entry_pipelined(case):
+    """Large enough for gdn_prefill_host to overlap its copies with the kernels: token
+    windows whose state carries hand the state on (dense) or head groups on separate
+    streams (packed). Bitwise the device entry's results, pinned or pageable."""
     import torch
     from hybrid_linear_attention_prefill_gb300 import gdn
     from hybrid_linear_attention_prefill_gb300.inputs import bf16_bits_to_f32
@@ -247,6 +249,12 @@ def test_host_entry_pipelined_over_head_groups(case):
                                        out, fin, B, T, inp.Hk, inp.Hv, inp.dk, inp.dv, 0))
         o_host = bf16_bits_to_f32(out.numpy().view(np.uint16))
         assert np.array_equal(o_host, o_dev) and np.array_equal(fin.numpy(), s_dev)
+    # no final state requested: the windows still hand the state on inside the library
+    out = np.zeros((Tt, inp.Hv, inp.dv), dtype=np.int16)
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens
+    gdn.check(gdn.gdn_prefill_host(inp.q.view(np.int16), inp.k.view(np.int16), inp.v.view(np.int16), inp.g,
+                                   inp.beta, cu, inp.init, out, None, B, T, inp.Hk, inp.Hv, inp.dk, inp.dv, 0))
+    assert np.array_equal(bf16_bits_to_f32(out.view(np.uint16)), o_dev)
 
 
 def test_misaligned_device_pointer_rejected():
