@@ -93,7 +93,8 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 const float* __restrict__ g, const float* __restrict__ beta,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_off,
                 __nv_bfloat16* __restrict__ ws, float* __restrict__ ws_rn, int* __restrict__ err, int B,
-                int T, int Hk, int Hv, int nc_dense, int norm_qk, int hk_base, int c_begin, int c_count) {
+                int T, int Hk, int Hv, int nc_dense, int norm_qk, int hk_base, int hk_count, int c_begin,
+                int c_count, int n_items) {
   using L = PrepSmem<DK>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -112,66 +113,52 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   float* rnq = rnk + kChunk;                                // 1/||q_t||
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // dense batches: CTA x covers chunk c_begin + x % c_count of sequence x / c_count (a window of
-  // each sequence's chunks; the whole sequence when c_begin = 0, c_count = nc_dense)
-  const int slot = cu == nullptr ? (int)(blockIdx.x / c_count) * nc_dense + c_begin + (int)(blockIdx.x % c_count)
-                                 : (int)blockIdx.x;
-  const int hk = hk_base + (int)blockIdx.y;
-  if (tid == 0) {  // the copies below are this CTA's first work; fetch their descriptors now
-    tc::prefetch_tensormap(&tm_k);
-    tc::prefetch_tensormap(&tm_q);
-  }
-
-  // ---- which sequence and chunk this slot is ---------------------------------
-  int b, c;
-  if (cu == nullptr) {
-    b = slot / nc_dense;
-    c = slot - b * nc_dense;
-    if (b >= B) return;
-  } else {
-    if (slot >= chunk_off[B]) return;
-    int lo = 0, hi = B;  // largest b with chunk_off[b] <= slot
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (chunk_off[mid] <= slot) lo = mid; else hi = mid;
-    }
-    b = lo;
-    c = slot - chunk_off[b];
-  }
-  const SeqChunk sq = seq_bounds(cu, b, T);
-  const long long t0 = sq.bos + (long long)c * kChunk;
-  const int n = min(kChunk, sq.len - c * kChunk);
-
-  // g and beta of one value head into buffer `buf` (zeros past the chunk's tokens), by
-  // warps 2 and 3, so that the start-up work of warps 0 and 1 (copies, TMEM) runs beside it
-  const int G = Hv / Hk;
-  auto prefetch_gb = [&](int gi, int buf) {
-    const int lt = tid - 64;
-    if (lt >= 0 && lt < kChunk) {
-      const bool ok = lt < n;
-      const size_t off = ok ? (size_t)(t0 + lt) * Hv + hk * G + gi : 0;
-      cp_async4(gbuf + buf * 2 * kChunk + lt, g + off, ok);
-      cp_async4(gbuf + buf * 2 * kChunk + kChunk + lt, beta + off, ok);
-    }
-    cp_async_commit();
-  };
-  prefetch_gb(0, 0);
-
-  // ---- the K and Q tiles by TMA (tokens past the end are zero); TMEM for the Grams
   constexpr int kKBlocks = DK > 64 ? 2 : 1;
   constexpr uint32_t kGramCols = 64;
-  if (tid == 0) {  // the copies first: the Grams wait for them
+  const int G = Hv / Hk;
+
+  // Items are (chunk slot, key head) pairs: item = x * hk_count + (key head - hk_base).  Dense
+  // batches: slot index x is chunk c_begin + x % c_count of sequence x / c_count (a window of
+  // each sequence's chunks; the whole sequence when c_begin = 0, c_count = nc_dense).  Packed
+  // batches: x is the slot, and slots past the last chunk are empty.
+  struct Item {
+    int slot, hk, b, c, n;
+    long long t0;
+  };
+  auto locate = [&](int item, Item& it) -> bool {
+    const int x = item / hk_count;
+    it.hk = hk_base + (item - x * hk_count);
+    if (cu == nullptr) {
+      it.b = x / c_count;
+      it.c = c_begin + (x - it.b * c_count);
+      if (it.b >= B) return false;
+      it.slot = it.b * nc_dense + it.c;
+    } else {
+      if (x >= chunk_off[B]) return false;
+      int lo = 0, hi = B;  // largest b with chunk_off[b] <= x
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (chunk_off[mid] <= x) lo = mid; else hi = mid;
+      }
+      it.b = lo;
+      it.c = x - chunk_off[lo];
+      it.slot = x;
+    }
+    const SeqChunk sq = seq_bounds(cu, it.b, T);
+    it.t0 = sq.bos + (long long)it.c * kChunk;
+    it.n = min(kChunk, sq.len - it.c * kChunk);
+    return true;
+  };
+
+  // ---- once per CTA: barriers, TMEM for the Grams -------------------------------------
+  if (tid == 0) {
+    tc::prefetch_tensormap(&tm_k);
+    tc::prefetch_tensormap(&tm_q);
     tc::mbar_init(&bar[0], 1);
     tc::mbar_init(&bar[1], 1);
     tc::fence_mbar_init();
-    tc::mbar_arrive_expect_tx(&bar[0], 2 * kKBlocks * 8192);
-#pragma unroll
-    for (int db = 0; db < kKBlocks; ++db) {
-      tc::tma_load_3d(KQ + db * 16384, &tm_k, 64 * db, hk, (int)t0, &bar[0]);
-      tc::tma_load_3d(KQ + db * 16384 + 8192, &tm_q, 64 * db, hk, (int)t0, &bar[0]);
-    }
   }
-  if (warp == 1) {  // beside thread 0's copies
+  if (warp == 1) {
     tc::tmem_alloc(tmem_slot, kGramCols);
     tc::tmem_relinquish();
   }
@@ -179,246 +166,293 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (!tc::mbar_wait(&bar[0], 0, 1u << 24)) atomicOr(err, 4);
-  // rows t >= n belong to the next sequence (or are past the end): clear them
-  if (n < kChunk) {
-    for (int e = tid; e < kKBlocks * 2 * (kChunk - n) * 8; e += kPrepThreads) {
-      const int piece = e & 7, rr = e >> 3;
-      const int r = n + rr % (kChunk - n), which = (rr / (kChunk - n)) & 1, db = rr / (2 * (kChunk - n));
-      *reinterpret_cast<uint4*>(KQ + db * 16384 + tc::sw128(64 * which + r, piece)) = make_uint4(0, 0, 0, 0);
-    }
-  }
-  tc::fence_proxy_async();  // the cleared rows are read by the tensor core
-  __syncthreads();
 
-  // ---- Grams on the tensor core: D = [K; Q] K^T (M = 128, N = 64, K = dk) -------
-  // Rows 0..63 of D are K K^T, rows 64..127 Q K^T; both operands are the K-major
-  // swizzled tile as loaded (the B operand is its first 64 rows).
-  if (tid == 0) {
-    tc::fence_after();
-    constexpr uint32_t kID = tc::idesc_bf16(128, 64, 0, 0);
-    const uint32_t kq = smem_u32(KQ);
-#pragma unroll
-    for (int ks = 0; ks < DK / 16; ++ks) {
-      const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-      tc::mma_bf16(tmem, tc::sdesc(kq + off, 16, 1024, tc::kSw128), tc::sdesc(kq + off, 16, 1024, tc::kSw128), kID,
-                   ks > 0);
-    }
-    tc::commit(&bar[1]);
-  }
-  // inverse norms of the k and q rows while the product runs
-  if (tid < 2 * kChunk) {
-    const float r = norm_qk ? tc::inv_norm(tc::row_sumsq_sw128<DK>(KQ, (tid & 63) + 64 * (tid >> 6))) : 1.f;
-    rnk[tid] = r;  // tid 0..63: k rows, 64..127: q rows (rnq = rnk + 64)
-    if (norm_qk) ws_rn[((size_t)slot * Hk + hk) * (2 * kChunk) + tid] = r;  // for the state carry
-  }
-  if (!tc::mbar_wait(&bar[1], 0, 1u << 24)) atomicOr(err, 4);
-  tc::fence_after();
-  // TMEM -> the fp32 Grams: warp w reads lanes 32 (w % 4) .. +31 (rows: 0..63 K, 64..127
-  // Q) and columns 32 (w / 4) .. +31
-  {
-    const int q4 = warp & 3, hf = warp >> 2;
-    float v[32];
-    tc::tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + 32 * hf, v);
-    float* dst = Gs + (q4 >> 1) * kChunk * LDF + (32 * (q4 & 1) + lane) * LDF + 32 * hf;
-#pragma unroll
-    for (int p = 0; p < 8; ++p)
-      *reinterpret_cast<float4*>(dst + 4 * p) = make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
-  }
-  tc::fence_before();
-  __syncthreads();  // Grams and norms visible; the tiles are dead from here on (A and Tm overwrite them)
+  // Persistent CTAs (two per SM) walk the items with the grid's stride.  While one item is
+  // worked on, the next one's key and query tiles are brought into L2, so its tile copy
+  // does not wait for DRAM.
+  uint32_t ph = 0;  // phase of bar[0] and bar[1]: each completes once per item worked on
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    Item cur;
+    if (!locate(item, cur)) continue;  // the same for every thread of the CTA
+    const int slot = cur.slot, hk = cur.hk, n = cur.n;
+    const long long t0 = cur.t0;
 
-  for (int gi = 0; gi < G; ++gi) {
-    const int h = hk * G + gi;
-    // this head's g / beta arrived by cp.async; start fetching the next head's
-    cp_async_wait<0>();
-    __syncthreads();
-    if (gi + 1 < G) prefetch_gb(gi + 1, (gi + 1) & 1);
-    // ---- gamma = inclusive cumsum of g in the chunk, in log2 units -------------------
-    // Every warp scans the 64 values in registers (lane l holds tokens l and l + 32), so
-    // no warp waits for another; the A/P build below takes its entries by shuffle.
-    const float* gb = gbuf + (gi & 1) * 2 * kChunk;  // [g 64 | beta 64]
-    float gl0 = gb[lane], gl1 = gb[lane + 32];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float u0 = __shfl_up_sync(0xffffffffu, gl0, o);
-      const float u1 = __shfl_up_sync(0xffffffffu, gl1, o);
-      if (lane >= o) { gl0 += u0; gl1 += u1; }
-    }
-    gl1 += __shfl_sync(0xffffffffu, gl0, 31);
-    gl0 *= 1.4426950408889634f;  // log2(e)
-    gl1 *= 1.4426950408889634f;
-
-    // ---- A (fp32) and P (bf16), 8 columns at a time, lower triangle only ----------
-    // Gamma[t][i] = 2^(gamma2_t - gamma2_i) with gamma2 = gamma log2(e): the exponent
-    // is never positive for i <= t.  A thread keeps one 8-column block (the CTA size is
-    // a multiple of 8), so its gamma and 1/||k|| columns are loaded once.
-    static_assert(kPrepThreads == 256, "two (row, column block) items per thread, rows tid / 8 and + 32");
-    const int c8 = (tid & 7) * 8;
-    float gcol[8], rcol[8];
-    {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {  // gamma of columns c8 .. c8 + 7 (tokens < 32 in gl0, the rest in gl1)
-        const float lo = __shfl_sync(0xffffffffu, gl0, (c8 + u) & 31);
-        const float hi = __shfl_sync(0xffffffffu, gl1, (c8 + u) & 31);
-        gcol[u] = c8 < 32 ? lo : hi;
+    // g and beta of one value head into buffer `buf` (zeros past the chunk's tokens), by
+    // warps 2 and 3, beside thread 0's copies
+    auto prefetch_gb = [&](int gi, int buf) {
+      const int lt = tid - 64;
+      if (lt >= 0 && lt < kChunk) {
+        const bool ok = lt < n;
+        const size_t off = ok ? (size_t)(t0 + lt) * Hv + hk * G + gi : 0;
+        cp_async4(gbuf + buf * 2 * kChunk + lt, g + off, ok);
+        cp_async4(gbuf + buf * 2 * kChunk + kChunk + lt, beta + off, ok);
       }
-      const float4 r0 = *reinterpret_cast<const float4*>(rnk + c8), r1 = *reinterpret_cast<const float4*>(rnk + c8 + 4);
-      rcol[0] = r0.x; rcol[1] = r0.y; rcol[2] = r0.z; rcol[3] = r0.w;
-      rcol[4] = r1.x; rcol[5] = r1.y; rcol[6] = r1.z; rcol[7] = r1.w;
-    }
-    // gamma of this thread's two rows, tid / 8 and tid / 8 + 32 (lane (tid / 8) % 32 of this warp)
-    const float grow0 = __shfl_sync(0xffffffffu, gl0, (tid >> 3) & 31);
-    const float grow1 = __shfl_sync(0xffffffffu, gl1, (tid >> 3) & 31);
-    for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
-      const int t = e >> 3;
-      float av[8], pv[8];
-      if (c8 <= t) {
-        const float gt = t < 32 ? grow0 : grow1, bt = gb[kChunk + t] * rnk[t], qt = rnq[t];
-        const float4 k0 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8);
-        const float4 k1 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8 + 4);
-        const float4 q0 = *reinterpret_cast<const float4*>(Gs + kChunk * LDF + t * LDF + c8);
-        const float4 q1 = *reinterpret_cast<const float4*>(Gs + kChunk * LDF + t * LDF + c8 + 4);
-        const float gk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-        const float gq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      cp_async_commit();
+    };
+    prefetch_gb(0, 0);
+
+    // ---- the K and Q tiles by TMA (tokens past the end are zero); the next item's into L2
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(&bar[0], 2 * kKBlocks * 8192);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = c8 + u;
-          const float dcy = i <= t ? exp2f(gt - gcol[u]) * rcol[u] : 0.f;
-          pv[u] = qt * dcy * gq[u];
-          av[u] = i < t ? bt * dcy * gk[u] : 0.f;
+      for (int db = 0; db < kKBlocks; ++db) {
+        tc::tma_load_3d(KQ + db * 16384, &tm_k, 64 * db, hk, (int)t0, &bar[0]);
+        tc::tma_load_3d(KQ + db * 16384 + 8192, &tm_q, 64 * db, hk, (int)t0, &bar[0]);
+      }
+      Item nx;
+      if (item + (int)gridDim.x < n_items && locate(item + (int)gridDim.x, nx)) {
+#pragma unroll
+        for (int db = 0; db < kKBlocks; ++db) {
+          tc::tma_prefetch_l2_3d(&tm_k, 64 * db, nx.hk, (int)nx.t0);
+          tc::tma_prefetch_l2_3d(&tm_q, 64 * db, nx.hk, (int)nx.t0);
         }
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) av[u] = pv[u] = 0.f;
-      }
-      *reinterpret_cast<float4*>(As + t * LDF + c8) = make_float4(av[0], av[1], av[2], av[3]);
-      *reinterpret_cast<float4*>(As + t * LDF + c8 + 4) = make_float4(av[4], av[5], av[6], av[7]);
-      *reinterpret_cast<uint4*>(Ps + t * LDB + c8) =
-          make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
-                     pack_bf16(pv[6], pv[7]));
-    }
-    if (gi == 0) {  // the blocks of Tm above the diagonal stay zero for every value head
-      for (int e = tid; e < kChunk * 16; e += kPrepThreads) {
-        const int t = e >> 4, c4 = (e & 15) * 4;
-        if ((c4 >> 4) > (t >> 4)) *reinterpret_cast<float4*>(Tms + t * LDF + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    __syncthreads();
-
-    // ---- Tm: the four 16 x 16 diagonal blocks by forward substitution --------
-    // Column j of a block: x_j = 1, then for i = j, j+1, ...: x_{i+1} = -acc_{i+1}
-    // after every later acc_t has absorbed A[t][i] x_i (right-looking order, so
-    // the dependent chain is one FMA per row).
-    if (tid < 64) {
-      const int blk = tid >> 4, j = tid & 15;
-      const float* Ab = As + 16 * blk * LDF + 16 * blk;
-      float x[16], accv[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) { x[i] = (i == j) ? 1.f : 0.f; accv[i] = 0.f; }
-#pragma unroll
-      for (int i = 0; i < 15; ++i) {
-        if (i > j) x[i] = -accv[i];
-#pragma unroll
-        for (int t = i + 1; t < 16; ++t) accv[t] = fmaf(Ab[t * LDF + i], x[i], accv[t]);
+    if (!tc::mbar_wait(&bar[0], ph, 1u << 24)) atomicOr(err, 4);
+    // rows t >= n belong to the next sequence (or are past the end): clear them
+    if (n < kChunk) {
+      for (int e = tid; e < kKBlocks * 2 * (kChunk - n) * 8; e += kPrepThreads) {
+        const int piece = e & 7, rr = e >> 3;
+        const int r = n + rr % (kChunk - n), which = (rr / (kChunk - n)) & 1, db = rr / (2 * (kChunk - n));
+        *reinterpret_cast<uint4*>(KQ + db * 16384 + tc::sw128(64 * which + r, piece)) = make_uint4(0, 0, 0, 0);
       }
-      if (15 > j) x[15] = -accv[15];
-      float* Tb = Tms + 16 * blk * LDF + 16 * blk;
+    }
+    tc::fence_proxy_async();  // the cleared rows are read by the tensor core
+    __syncthreads();
+
+    // ---- Grams on the tensor core: D = [K; Q] K^T (M = 128, N = 64, K = dk) -------
+    // Rows 0..63 of D are K K^T, rows 64..127 Q K^T; both operands are the K-major
+    // swizzled tile as loaded (the B operand is its first 64 rows).
+    if (tid == 0) {
+      tc::fence_after();
+      constexpr uint32_t kID = tc::idesc_bf16(128, 64, 0, 0);
+      const uint32_t kq = smem_u32(KQ);
 #pragma unroll
-      for (int t = 0; t < 16; ++t) Tb[t * LDF + j] = x[t];
+      for (int ks = 0; ks < DK / 16; ++ks) {
+        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+        tc::mma_bf16(tmem, tc::sdesc(kq + off, 16, 1024, tc::kSw128), tc::sdesc(kq + off, 16, 1024, tc::kSw128), kID,
+                     ks > 0);
+      }
+      tc::commit(&bar[1]);
     }
-    __syncthreads();
-
-    // ---- merge 16 -> 32: T[o+16.., o..] = -T22 (A21 T11), o = 0 and 32 -------
-    // Warp w < 4 forms the 8-column tile nt = w % 2 of block o = 32 (w / 2): its column
-    // tile of W = A21 T11 is all that its tile of T21 = -T22 W needs.
-    if (warp < 4) {
-      const int o = 32 * (warp >> 1), nt = warp & 1;
-      float* W = Wt + 16 * (warp >> 1) * LDW;  // this block's 16 x 16 part of the buffer
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_f32x3(acc, As, LDF, o + 16, o, Tms, LDF, o, o + 8 * nt, lane);
-      store_tile(W, LDW, 0, 8 * nt, acc, 1.f, lane);
-      __syncwarp();
-      float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_f32x3(acc2, Tms, LDF, o + 16, o + 16, W, LDW, 0, 8 * nt, lane);
-      store_tile(Tms, LDF, o + 16, o + 8 * nt, acc2, -1.f, lane);
+    // inverse norms of the k and q rows while the product runs
+    if (tid < 2 * kChunk) {
+      const float r = norm_qk ? tc::inv_norm(tc::row_sumsq_sw128<DK>(KQ, (tid & 63) + 64 * (tid >> 6))) : 1.f;
+      rnk[tid] = r;  // tid 0..63: k rows, 64..127: q rows (rnq = rnk + 64)
+      if (norm_qk) ws_rn[((size_t)slot * Hk + hk) * (2 * kChunk) + tid] = r;  // for the state carry
     }
-    __syncthreads();
-
-    // ---- merge 32 -> 64: T[32.., 0..32] = -T[32..,32..] (A[32..,0..32] T[0..32,0..32]) ----
+    if (!tc::mbar_wait(&bar[1], ph, 1u << 24)) atomicOr(err, 4);
+    tc::fence_after();
+    // TMEM -> the fp32 Grams: warp w reads lanes 32 (w % 4) .. +31 (rows: 0..63 K, 64..127
+    // Q) and columns 32 (w / 4) .. +31
     {
-      const int mt = warp >> 2, nt = warp & 3;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int q4 = warp & 3, hf = warp >> 2;
+      float v[32];
+      tc::tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + 32 * hf, v);
+      float* dst = Gs + (q4 >> 1) * kChunk * LDF + (32 * (q4 & 1) + lane) * LDF + 32 * hf;
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) mma_f32x3(acc, As, LDF, 32 + 16 * mt, 16 * kk, Tms, LDF, 16 * kk, 8 * nt, lane);
-      store_tile(Wt, LDW, 16 * mt, 8 * nt, acc, 1.f, lane);
+      for (int p = 0; p < 8; ++p)
+        *reinterpret_cast<float4*>(dst + 4 * p) = make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
+    }
+    tc::fence_before();
+    __syncthreads();  // Grams and norms visible; the tiles are dead from here on (A and Tm overwrite them)
+
+
+    for (int gi = 0; gi < G; ++gi) {
+      const int h = hk * G + gi;
+      // this head's g / beta arrived by cp.async; start fetching the next head's
+      cp_async_wait<0>();
       __syncthreads();
-      float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+      if (gi + 1 < G) prefetch_gb(gi + 1, (gi + 1) & 1);
+      // ---- gamma = inclusive cumsum of g in the chunk, in log2 units -------------------
+      // Every warp scans the 64 values in registers (lane l holds tokens l and l + 32), so
+      // no warp waits for another; the A/P build below takes its entries by shuffle.
+      const float* gb = gbuf + (gi & 1) * 2 * kChunk;  // [g 64 | beta 64]
+      float gl0 = gb[lane], gl1 = gb[lane + 32];
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
-        mma_f32x3(acc2, Tms, LDF, 32 + 16 * mt, 32 + 16 * kk, Wt, LDW, 16 * kk, 8 * nt, lane);
-      store_tile(Tms, LDF, 32 + 16 * mt, 8 * nt, acc2, -1.f, lane);
-    }
-    __syncthreads();
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u0 = __shfl_up_sync(0xffffffffu, gl0, o);
+        const float u1 = __shfl_up_sync(0xffffffffu, gl1, o);
+        if (lane >= o) { gl0 += u0; gl1 += u1; }
+      }
+      gl1 += __shfl_sync(0xffffffffu, gl0, 31);
+      gl0 *= 1.4426950408889634f;  // log2(e)
+      gl1 *= 1.4426950408889634f;
 
-    // ---- bf16 Tm: to shared (for PT) and to the workspace ---------------------
-    __nv_bfloat16* wsT = ws + ((size_t)slot * Hv + h) * (2 * kWsTileElems);
-    __nv_bfloat16* wsPT = wsT + kWsTileElems;
-    for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
-      const int r = e >> 3, p = e & 7;
-      const float* src = Tms + r * LDF + 8 * p;
-      uint4 v;
-      v.x = pack_bf16(src[0], src[1]);
-      v.y = pack_bf16(src[2], src[3]);
-      v.z = pack_bf16(src[4], src[5]);
-      v.w = pack_bf16(src[6], src[7]);
-      *reinterpret_cast<uint4*>(Tmb + r * LDB + 8 * p) = v;
-      *reinterpret_cast<uint4*>(wsT + r * kChunk + 8 * p) = v;
-    }
-    __syncthreads();
+      // ---- A (fp32) and P (bf16), 8 columns at a time, lower triangle only ----------
+      // Gamma[t][i] = 2^(gamma2_t - gamma2_i) with gamma2 = gamma log2(e): the exponent
+      // is never positive for i <= t.  A thread keeps one 8-column block (the CTA size is
+      // a multiple of 8), so its gamma and 1/||k|| columns are loaded once.
+      static_assert(kPrepThreads == 256, "two (row, column block) items per thread, rows tid / 8 and + 32");
+      const int c8 = (tid & 7) * 8;
+      float gcol[8], rcol[8];
+      {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // gamma of columns c8 .. c8 + 7 (tokens < 32 in gl0, the rest in gl1)
+          const float lo = __shfl_sync(0xffffffffu, gl0, (c8 + u) & 31);
+          const float hi = __shfl_sync(0xffffffffu, gl1, (c8 + u) & 31);
+          gcol[u] = c8 < 32 ? lo : hi;
+        }
+        const float4 r0 = *reinterpret_cast<const float4*>(rnk + c8), r1 = *reinterpret_cast<const float4*>(rnk + c8 + 4);
+        rcol[0] = r0.x; rcol[1] = r0.y; rcol[2] = r0.z; rcol[3] = r0.w;
+        rcol[4] = r1.x; rcol[5] = r1.y; rcol[6] = r1.z; rcol[7] = r1.w;
+      }
+      // gamma of this thread's two rows, tid / 8 and tid / 8 + 32 (lane (tid / 8) % 32 of this warp)
+      const float grow0 = __shfl_sync(0xffffffffu, gl0, (tid >> 3) & 31);
+      const float grow1 = __shfl_sync(0xffffffffu, gl1, (tid >> 3) & 31);
+      for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
+        const int t = e >> 3;
+        float av[8], pv[8];
+        if (c8 <= t) {
+          const float gt = t < 32 ? grow0 : grow1, bt = gb[kChunk + t] * rnk[t], qt = rnq[t];
+          const float4 k0 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8);
+          const float4 k1 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8 + 4);
+          const float4 q0 = *reinterpret_cast<const float4*>(Gs + kChunk * LDF + t * LDF + c8);
+          const float4 q1 = *reinterpret_cast<const float4*>(Gs + kChunk * LDF + t * LDF + c8 + 4);
+          const float gk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+          const float gq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int i = c8 + u;
+            const float dcy = i <= t ? exp2f(gt - gcol[u]) * rcol[u] : 0.f;
+            pv[u] = qt * dcy * gq[u];
+            av[u] = i < t ? bt * dcy * gk[u] : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) av[u] = pv[u] = 0.f;
+        }
+        *reinterpret_cast<float4*>(As + t * LDF + c8) = make_float4(av[0], av[1], av[2], av[3]);
+        *reinterpret_cast<float4*>(As + t * LDF + c8 + 4) = make_float4(av[4], av[5], av[6], av[7]);
+        *reinterpret_cast<uint4*>(Ps + t * LDB + c8) =
+            make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
+                       pack_bf16(pv[6], pv[7]));
+      }
+      if (gi == 0) {  // the blocks of Tm above the diagonal stay zero for every value head
+        for (int e = tid; e < kChunk * 16; e += kPrepThreads) {
+          const int t = e >> 4, c4 = (e & 15) * 4;
+          if ((c4 >> 4) > (t >> 4)) *reinterpret_cast<float4*>(Tms + t * LDF + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      __syncthreads();
 
-    // ---- PT = P Tm (lower triangular); warp w: rows 16 (w/2).., column pairs ---
-    {
-      const int mi = warp >> 1, m = lane >> 3;
-      float acc[4][4];
+      // ---- Tm: the four 16 x 16 diagonal blocks by forward substitution --------
+      // Column j of a block: x_j = 1, then for i = j, j+1, ...: x_{i+1} = -acc_{i+1}
+      // after every later acc_t has absorbed A[t][i] x_i (right-looking order, so
+      // the dependent chain is one FMA per row).
+      if (tid < 64) {
+        const int blk = tid >> 4, j = tid & 15;
+        const float* Ab = As + 16 * blk * LDF + 16 * blk;
+        float x[16], accv[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        for (int i = 0; i < 16; ++i) { x[i] = (i == j) ? 1.f : 0.f; accv[i] = 0.f; }
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        if (kk <= mi) {
-          uint32_t a[4];
-          ldsm_x4(a, Ps + (16 * mi + 8 * (m & 1) + (lane & 7)) * LDB + 16 * kk + 8 * (m >> 1));
+        for (int i = 0; i < 15; ++i) {
+          if (i > j) x[i] = -accv[i];
 #pragma unroll
-          for (int pp = 0; pp < 2; ++pp) {
-            const int p = 2 * (warp & 1) + pp;  // column pair: columns 16 p .. 16 p + 15
-            if (p <= kk) {
-              uint32_t bb[4];
-              ldsm_x4_t(bb, Tmb + (16 * kk + 8 * (m & 1) + (lane & 7)) * LDB + 8 * (2 * p + (m >> 1)));
-              mma_bf16(acc[2 * pp], a, bb[0], bb[1]);
-              mma_bf16(acc[2 * pp + 1], a, bb[2], bb[3]);
+          for (int t = i + 1; t < 16; ++t) accv[t] = fmaf(Ab[t * LDF + i], x[i], accv[t]);
+        }
+        if (15 > j) x[15] = -accv[15];
+        float* Tb = Tms + 16 * blk * LDF + 16 * blk;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) Tb[t * LDF + j] = x[t];
+      }
+      __syncthreads();
+
+      // ---- merge 16 -> 32: T[o+16.., o..] = -T22 (A21 T11), o = 0 and 32 -------
+      // Warp w < 4 forms the 8-column tile nt = w % 2 of block o = 32 (w / 2): its column
+      // tile of W = A21 T11 is all that its tile of T21 = -T22 W needs.
+      if (warp < 4) {
+        const int o = 32 * (warp >> 1), nt = warp & 1;
+        float* W = Wt + 16 * (warp >> 1) * LDW;  // this block's 16 x 16 part of the buffer
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f32x3(acc, As, LDF, o + 16, o, Tms, LDF, o, o + 8 * nt, lane);
+        store_tile(W, LDW, 0, 8 * nt, acc, 1.f, lane);
+        __syncwarp();
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f32x3(acc2, Tms, LDF, o + 16, o + 16, W, LDW, 0, 8 * nt, lane);
+        store_tile(Tms, LDF, o + 16, o + 8 * nt, acc2, -1.f, lane);
+      }
+      __syncthreads();
+
+      // ---- merge 32 -> 64: T[32.., 0..32] = -T[32..,32..] (A[32..,0..32] T[0..32,0..32]) ----
+      {
+        const int mt = warp >> 2, nt = warp & 3;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) mma_f32x3(acc, As, LDF, 32 + 16 * mt, 16 * kk, Tms, LDF, 16 * kk, 8 * nt, lane);
+        store_tile(Wt, LDW, 16 * mt, 8 * nt, acc, 1.f, lane);
+        __syncthreads();
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          mma_f32x3(acc2, Tms, LDF, 32 + 16 * mt, 32 + 16 * kk, Wt, LDW, 16 * kk, 8 * nt, lane);
+        store_tile(Tms, LDF, 32 + 16 * mt, 8 * nt, acc2, -1.f, lane);
+      }
+      __syncthreads();
+
+      // ---- bf16 Tm: to shared (for PT) and to the workspace ---------------------
+      __nv_bfloat16* wsT = ws + ((size_t)slot * Hv + h) * (2 * kWsTileElems);
+      __nv_bfloat16* wsPT = wsT + kWsTileElems;
+      for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
+        const int r = e >> 3, p = e & 7;
+        const float* src = Tms + r * LDF + 8 * p;
+        uint4 v;
+        v.x = pack_bf16(src[0], src[1]);
+        v.y = pack_bf16(src[2], src[3]);
+        v.z = pack_bf16(src[4], src[5]);
+        v.w = pack_bf16(src[6], src[7]);
+        *reinterpret_cast<uint4*>(Tmb + r * LDB + 8 * p) = v;
+        *reinterpret_cast<uint4*>(wsT + r * kChunk + 8 * p) = v;
+      }
+      __syncthreads();
+
+      // ---- PT = P Tm (lower triangular); warp w: rows 16 (w/2).., column pairs ---
+      {
+        const int mi = warp >> 1, m = lane >> 3;
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if (kk <= mi) {
+            uint32_t a[4];
+            ldsm_x4(a, Ps + (16 * mi + 8 * (m & 1) + (lane & 7)) * LDB + 16 * kk + 8 * (m >> 1));
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+              const int p = 2 * (warp & 1) + pp;  // column pair: columns 16 p .. 16 p + 15
+              if (p <= kk) {
+                uint32_t bb[4];
+                ldsm_x4_t(bb, Tmb + (16 * kk + 8 * (m & 1) + (lane & 7)) * LDB + 8 * (2 * p + (m >> 1)));
+                mma_bf16(acc[2 * pp], a, bb[0], bb[1]);
+                mma_bf16(acc[2 * pp + 1], a, bb[2], bb[3]);
+              }
             }
           }
         }
-      }
-      __syncthreads();  // every warp has read P before it is overwritten with PT
-      const int r0 = 16 * mi + (lane >> 2);
+        __syncthreads();  // every warp has read P before it is overwritten with PT
+        const int r0 = 16 * mi + (lane >> 2);
 #pragma unroll
-      for (int pp = 0; pp < 2; ++pp) {
+        for (int pp = 0; pp < 2; ++pp) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int cc = 16 * (2 * (warp & 1) + pp) + 8 * hh + 2 * (lane & 3);
-          *reinterpret_cast<uint32_t*>(Ps + r0 * LDB + cc) = pack_bf16(acc[2 * pp + hh][0], acc[2 * pp + hh][1]);
-          *reinterpret_cast<uint32_t*>(Ps + (r0 + 8) * LDB + cc) =
-              pack_bf16(acc[2 * pp + hh][2], acc[2 * pp + hh][3]);
+          for (int hh = 0; hh < 2; ++hh) {
+            const int cc = 16 * (2 * (warp & 1) + pp) + 8 * hh + 2 * (lane & 3);
+            *reinterpret_cast<uint32_t*>(Ps + r0 * LDB + cc) = pack_bf16(acc[2 * pp + hh][0], acc[2 * pp + hh][1]);
+            *reinterpret_cast<uint32_t*>(Ps + (r0 + 8) * LDB + cc) =
+                pack_bf16(acc[2 * pp + hh][2], acc[2 * pp + hh][3]);
+          }
         }
       }
+      __syncthreads();
+      for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
+        const int r = e >> 3, p = e & 7;
+        *reinterpret_cast<uint4*>(wsPT + r * kChunk + 8 * p) =
+            *reinterpret_cast<const uint4*>(Ps + r * LDB + 8 * p);
+      }
+      __syncthreads();
     }
-    __syncthreads();
-    for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
-      const int r = e >> 3, p = e & 7;
-      *reinterpret_cast<uint4*>(wsPT + r * kChunk + 8 * p) =
-          *reinterpret_cast<const uint4*>(Ps + r * LDB + 8 * p);
-    }
+    ph ^= 1;
+    tc::fence_proxy_async();  // the next item's tile copy overwrites what this one left in shared memory
     __syncthreads();
   }
   if (warp == 1) tc::tmem_dealloc(tmem, kGramCols);
@@ -506,11 +540,20 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   cudaError_t e = set_smem_limit_once<gdn_prep_kernel<DK>>(L::bytes);
   if (e != cudaSuccess) return e;
   if (cu == nullptr && (c_begin < 0 || c_count <= 0 || c_begin + c_count > nc_dense)) return cudaErrorInvalidValue;
-  // key heads hk_base .. hk_base + hk_count - 1; dense: B sequences x c_count chunks
-  dim3 grid(cu == nullptr ? (unsigned)B * (unsigned)c_count : (unsigned)nslots, hk_count);
-  gdn_prep_kernel<DK><<<grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
+  // items: key heads hk_base .. hk_base + hk_count - 1 of B sequences x c_count chunks (dense)
+  // or of every slot (packed); persistent CTAs, two per SM
+  const long long n_items = (cu == nullptr ? (long long)B * c_count : (long long)nslots) * hk_count;
+  if (n_items <= 0) return cudaSuccess;
+  if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const long long grid = n_items < 2LL * sms ? n_items : 2LL * sms;
+  gdn_prep_kernel<DK><<<(unsigned)grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
                                                            static_cast<__nv_bfloat16*>(ws), ws_rn, err, B, T, Hk, Hv,
-                                                           nc_dense, norm_qk, hk_base, c_begin, c_count);
+                                                           nc_dense, norm_qk, hk_base, hk_count, c_begin,
+                                                           c_count, (int)n_items);
   return cudaGetLastError();
 }
 

@@ -148,6 +148,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, i
       : "memory");
 }
 
+// Bring a tile into L2 ahead of a later load of it (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(map), "r"(x), "r"(y),
+               "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(map) : "memory");
 }
