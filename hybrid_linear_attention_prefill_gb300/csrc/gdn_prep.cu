@@ -150,14 +150,49 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     return true;
   };
 
-  // ---- once per CTA: barriers, TMEM for the Grams -------------------------------------
+  // g and beta of value head gi of an item into buffer `buf` (zeros past the chunk's
+  // tokens), by warps 2 and 3, beside thread 0's copies
+  auto load_gb = [&](const Item& it, int gi, int buf) {
+    const int lt = tid - 64;
+    if (lt >= 0 && lt < kChunk) {
+      const bool ok = lt < it.n;
+      const size_t off = ok ? (size_t)(it.t0 + lt) * Hv + it.hk * G + gi : 0;
+      cp_async4(gbuf + buf * 2 * kChunk + lt, g + off, ok);
+      cp_async4(gbuf + buf * 2 * kChunk + kChunk + lt, beta + off, ok);
+    }
+    cp_async_commit();
+  };
+  // An item's K and Q tiles by TMA (tokens past the end are zero), and the tiles of the
+  // CTA's following item into L2 (thread 0)
+  auto load_tiles = [&](int item, const Item& it) {
+    tc::mbar_arrive_expect_tx(&bar[0], 2 * kKBlocks * 8192);
+#pragma unroll
+    for (int db = 0; db < kKBlocks; ++db) {
+      tc::tma_load_3d(KQ + db * 16384, &tm_k, 64 * db, it.hk, (int)it.t0, &bar[0]);
+      tc::tma_load_3d(KQ + db * 16384 + 8192, &tm_q, 64 * db, it.hk, (int)it.t0, &bar[0]);
+    }
+    Item nx;
+    if (item + (int)gridDim.x < n_items && locate(item + (int)gridDim.x, nx)) {
+#pragma unroll
+      for (int db = 0; db < kKBlocks; ++db) {
+        tc::tma_prefetch_l2_3d(&tm_k, 64 * db, nx.hk, (int)nx.t0);
+        tc::tma_prefetch_l2_3d(&tm_q, 64 * db, nx.hk, (int)nx.t0);
+      }
+    }
+  };
+
+  // ---- once per CTA: barriers, TMEM for the Grams; the first item's loads beside them ---
+  Item first;
+  const bool first_ok = locate(blockIdx.x, first);
   if (tid == 0) {
     tc::prefetch_tensormap(&tm_k);
     tc::prefetch_tensormap(&tm_q);
     tc::mbar_init(&bar[0], 1);
     tc::mbar_init(&bar[1], 1);
     tc::fence_mbar_init();
+    if (first_ok) load_tiles(blockIdx.x, first);
   }
+  if (first_ok) load_gb(first, 0, 0);
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, kGramCols);
     tc::tmem_relinquish();
@@ -175,38 +210,11 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     Item cur;
     if (!locate(item, cur)) continue;  // the same for every thread of the CTA
     const int slot = cur.slot, hk = cur.hk, n = cur.n;
-    const long long t0 = cur.t0;
 
-    // g and beta of one value head into buffer `buf` (zeros past the chunk's tokens), by
-    // warps 2 and 3, beside thread 0's copies
-    auto prefetch_gb = [&](int gi, int buf) {
-      const int lt = tid - 64;
-      if (lt >= 0 && lt < kChunk) {
-        const bool ok = lt < n;
-        const size_t off = ok ? (size_t)(t0 + lt) * Hv + hk * G + gi : 0;
-        cp_async4(gbuf + buf * 2 * kChunk + lt, g + off, ok);
-        cp_async4(gbuf + buf * 2 * kChunk + kChunk + lt, beta + off, ok);
-      }
-      cp_async_commit();
-    };
-    prefetch_gb(0, 0);
-
-    // ---- the K and Q tiles by TMA (tokens past the end are zero); the next item's into L2
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(&bar[0], 2 * kKBlocks * 8192);
-#pragma unroll
-      for (int db = 0; db < kKBlocks; ++db) {
-        tc::tma_load_3d(KQ + db * 16384, &tm_k, 64 * db, hk, (int)t0, &bar[0]);
-        tc::tma_load_3d(KQ + db * 16384 + 8192, &tm_q, 64 * db, hk, (int)t0, &bar[0]);
-      }
-      Item nx;
-      if (item + (int)gridDim.x < n_items && locate(item + (int)gridDim.x, nx)) {
-#pragma unroll
-        for (int db = 0; db < kKBlocks; ++db) {
-          tc::tma_prefetch_l2_3d(&tm_k, 64 * db, nx.hk, (int)nx.t0);
-          tc::tma_prefetch_l2_3d(&tm_q, 64 * db, nx.hk, (int)nx.t0);
-        }
-      }
+    // the loads of this item (the first item's went out before the set-up barrier)
+    if (item != (int)blockIdx.x) {
+      load_gb(cur, 0, 0);
+      if (tid == 0) load_tiles(item, cur);
     }
     if (!tc::mbar_wait(&bar[0], ph, 1u << 24)) atomicOr(err, 4);
     // rows t >= n belong to the next sequence (or are past the end): clear them
@@ -263,7 +271,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       // this head's g / beta arrived by cp.async; start fetching the next head's
       cp_async_wait<0>();
       __syncthreads();
-      if (gi + 1 < G) prefetch_gb(gi + 1, (gi + 1) & 1);
+      if (gi + 1 < G) load_gb(cur, gi + 1, (gi + 1) & 1);
       // ---- gamma = inclusive cumsum of g in the chunk, in log2 units -------------------
       // Every warp scans the 64 values in registers (lane l holds tokens l and l + 32), so
       // no warp waits for another; the A/P build below takes its entries by shuffle.
