@@ -16,7 +16,8 @@
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, cudaStream_t);
+                        void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, int,
+                        cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
@@ -246,6 +247,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   const bool whole = c0 == 0 && c1 == nc_dense;
   if (!packed && (c0 < 0 || c1 > nc_dense || c0 >= c1) && nc_dense > 0) return GDN_ERR_ARG;
   const int cc0 = packed ? 0 : c0, cc1 = packed ? INT_MAX : c1;  // the chain's window
+  // a whole problem's preparation kernel has the device to itself; a piece of the host
+  // entry's pipeline runs beside other pieces' kernels
+  const int alone = whole && h0 == 0 && h1 == Hv && phases == 3;
   float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
   cudaError_t e = cudaSuccess;
   if (packed && table && (phases & 1)) {
@@ -258,9 +262,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   if (nslots > 0x7fffffffLL) return GDN_ERR_ARG;
   if (nslots > 0 && (phases & 1)) {
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, alone, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, alone, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, alone, st); break;
     }
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }

@@ -529,7 +529,7 @@ template <int DK>
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const float* beta,
                         const int32_t* cu, const int32_t* chunk_off, void* ws, float* ws_rn, int* err, int B, int T,
                         int Hk, int Hv, int nslots, int nc_dense, int norm_qk, int hk_base, int hk_count,
-                        int c_begin, int c_count, cudaStream_t st) {
+                        int c_begin, int c_count, int persistent, cudaStream_t st) {
   using L = PrepSmem<DK>;
   PFN_cuTensorMapEncodeTiled_v12000 enc = prep_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -549,7 +549,9 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   if (e != cudaSuccess) return e;
   if (cu == nullptr && (c_begin < 0 || c_count <= 0 || c_begin + c_count > nc_dense)) return cudaErrorInvalidValue;
   // items: key heads hk_base .. hk_base + hk_count - 1 of B sequences x c_count chunks (dense)
-  // or of every slot (packed); persistent CTAs, two per SM
+  // or of every slot (packed).  With the device to itself: persistent CTAs, two per SM.  Beside
+  // other kernels (the host entry's pipelines) a CTA per item, so that the hardware spreads the
+  // items over whatever SMs come free.
   const long long n_items = (cu == nullptr ? (long long)B * c_count : (long long)nslots) * hk_count;
   if (n_items <= 0) return cudaSuccess;
   if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -557,7 +559,7 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  const long long grid = n_items < 2LL * sms ? n_items : 2LL * sms;
+  const long long grid = persistent && n_items > 2LL * sms ? 2LL * sms : n_items;
   gdn_prep_kernel<DK><<<(unsigned)grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
                                                            static_cast<__nv_bfloat16*>(ws), ws_rn, err, B, T, Hk, Hv,
                                                            nc_dense, norm_qk, hk_base, hk_count, c_begin,
@@ -573,7 +575,7 @@ cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_o
 #define GDN_INST_PREP(DK)                                                                                  \
   template cudaError_t launch_prep<DK>(const void*, const void*, const float*, const float*, const int32_t*, \
                                        const int32_t*, void*, float*, int*, int, int, int, int, int, int, int,  \
-                                       int, int, int, int, cudaStream_t);
+                                       int, int, int, int, int, cudaStream_t);
 GDN_INST_PREP(32)
 GDN_INST_PREP(64)
 GDN_INST_PREP(128)

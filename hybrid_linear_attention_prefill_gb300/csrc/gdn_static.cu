@@ -31,7 +31,8 @@
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, cudaStream_t);
+                        void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, int,
+                        cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
@@ -104,9 +105,9 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   }
   if (nslots > 0) {
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
     }
     if (e != cudaSuccess) return GDN_ERR_LAUNCH;
   }
