@@ -85,7 +85,11 @@ int gdn_last_cuda_error(void);
  *
  * Memory.  The library keeps a per-device, grow-only workspace (allocated on the
  * first call that needs more; about 16 KB per 64-token chunk and value head).
- * After a call at the largest size, later calls allocate nothing.
+ * After a call at the largest size, later calls allocate nothing.  gdn_prefill,
+ * gdn_prefill_ex and gdn_prefill_host calls on one device share that workspace
+ * (and gdn_prefill_host's staging area): calls whose GPU work could overlap
+ * (different streams, or host threads without ordering) must be ordered by the
+ * caller, or use gdn_prefill_ws with a workspace each.
  *
  * Long prompts with few heads.  The chunks of a sequence are processed in order,
  * so a dense batch (cu_seqlens == NULL) whose B * Hv * dv / 32 state-carry blocks
