@@ -45,6 +45,10 @@ def _run_ex(gdn, inp, flags):
     dict(lengths=[70, 0, 200, 5], Hk=2, Hv=4, dk=128, dv=128, init_std=0.1),
     dict(B=2, T=130, Hk=1, Hv=2, dk=64, dv=64),
     dict(B=1, T=100, Hk=1, Hv=1, dk=32, dv=32),
+    # more (chunk, key head) items than preparation CTAs: each CTA works on several, writing
+    # every item's inverse norms
+    dict(B=1, T=4096, Hk=16, Hv=32, dk=128, dv=128),
+    dict(lengths=[1500, 0, 900, 77, 640], Hk=8, Hv=16, dk=64, dv=64, init_std=0.1),
 ])
 def test_in_kernel_normalisation_matches_oracle(gdn, case):
     import oracle
