@@ -124,7 +124,7 @@ int gdn_prefill(const void *q, const void *k, const void *v,
  * 8 MB or more (q, k and v together) the copies overlap the kernels, on
  * library-owned streams that are joined back into `stream`:
  *   - equal-length batches: 2 to 8 windows of whole 64-token chunks (about 16
- *     chunks each).  The copies of one window overlap the kernels of the previous
+ *     chunks each, the last one half as many).  The copies of one window overlap the kernels of the previous
  *     one and the copy-back of earlier ones; each window's state carry starts from
  *     the state the previous window left (kept on the device in fp32);
  *   - packed batches: up to four groups of whole key heads, whose state carries
