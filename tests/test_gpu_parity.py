@@ -85,7 +85,7 @@ def test_workload_t16381_carry_sampled():
 
 # ---- edge cases ------------------------------------------------------------------
 
-@pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 127, 200])
+@pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257, 383])
 def test_ragged_lengths(T):
     check_full(make_gdn_inputs(B=2, T=T, Hk=2, Hv=4, dk=128, dv=128, seed=T, init_std=0.1))
 
@@ -101,7 +101,7 @@ def test_head_groups(Hk, Hv):
 
 
 def test_packed_with_empty_sequences():
-    inp = make_gdn_inputs(lengths=[0, 70, 0, 1, 64, 130, 0], Hk=2, Hv=4, dk=128, dv=128, seed=7,
+    inp = make_gdn_inputs(lengths=[0, 70, 0, 1, 64, 130, 0, 300], Hk=2, Hv=4, dk=128, dv=128, seed=7,
                           init_std=0.2)
     o, s = check_full(inp)
     for b in (0, 2, 6):  # empty sequences return their initial state exactly
