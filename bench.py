@@ -173,10 +173,30 @@ def to_device(inp, torch, dev):
                 init=None if inp.init is None else t(inp.init))
 
 
+def host_cores():
+    """Core counts of the host: what the C++ runtime would report as its hardware
+    concurrency (all online CPUs) and what `nproc` reports (the CPUs this process may
+    run on)."""
+    hw = os.cpu_count() or 1
+    try:
+        avail = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        avail = hw
+    return hw, avail
+
+
+def workload_config(args, inp, world):
+    """The `config` object both arms print for the same workload."""
+    return {"workload": args.workload, "B": inp.B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv, "dk": inp.dk,
+            "dv": inp.dv, "tokens": inp.total_tokens, "l2": "flushed between timed steps (256 MB write)",
+            "parallelism": f"replicas x{world}", "levels": args.levels}
+
+
 def cpu_baseline_oracle(inp, target_s=1.5):
     """Time the float64 oracle as it stands on the host cores on a bounded sample:
     all value heads of the first `n` tokens of every sequence, n sized to ~target_s of
-    wall time; when the whole workload takes less, it is run again until ~target_s."""
+    wall time; when the whole workload takes less, it is run again until ~target_s.
+    The same sample is then run once on a single thread."""
     import oracle
 
     cores = oracle.num_cpus()
@@ -194,9 +214,16 @@ def cpu_baseline_oracle(inp, target_s=1.5):
         oracle.prefill_inputs(sub, want_final=True, nthreads=cores)
         dt += time.perf_counter() - t0
         runs += 1
+    t0 = time.perf_counter()
+    oracle.prefill_inputs(sub, want_final=True, nthreads=1)
+    dt1 = time.perf_counter() - t0
+    hw, avail = host_cores()
     return {"value": runs * sub.total_tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "hardware_concurrency": hw, "nproc": avail,
+            "single_thread": {"value": sub.total_tokens / dt1, "unit": "tokens/s", "wall_s": round(dt1, 3)},
             "sample": f"first {sub.total_tokens} of {inp.total_tokens} tokens, all {inp.Hv} value heads, "
-                      f"float64 token loop, {runs} run(s), {dt:.2f} s wall"}
+                      f"float64 token loop, {runs} run(s), {dt:.2f} s wall on {cores} threads; "
+                      f"once on 1 thread, {dt1:.2f} s wall"}
 
 
 def slice_tokens(inp, n):
@@ -353,10 +380,7 @@ def run_gpu_arm(args):
             "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "B": B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv,
-                       "dk": inp.dk, "dv": inp.dv, "tokens": Tt,
-                       "l2": "flushed between timed steps (256 MB write)",
-                       "parallelism": f"replicas x{world}", "levels": args.levels},
+            "config": workload_config(args, inp, world),
             "roofline": roofline, "path_roofline": path_roof,
             "kernels_us": {k: round(v * 1e3, 2) for k, v in kernels.items()},
             "ms_per_step_min": min(step_ms), "wall_s": round(wall, 3),
@@ -542,9 +566,9 @@ def run_reference_arm(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "B": inp.B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv,
-                   "dk": inp.dk, "dv": inp.dv, "tokens": inp.total_tokens},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "config": workload_config(args, inp, int(os.environ.get("WORLD_SIZE", "1"))),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "hardware_concurrency": host_cores()[0], "nproc": host_cores()[1]},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

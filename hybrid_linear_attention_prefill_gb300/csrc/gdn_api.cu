@@ -7,10 +7,12 @@
 // CUDA Graph paragraph; "Open-Jev-27B-v1.1 native text worker", "Build and
 // serve" and "Prepare the checkpoint").
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
+#include "gdn_internal.h"
 #include <climits>
 
 namespace gdn {
@@ -18,7 +20,7 @@ template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
                         void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, int,
                         cudaStream_t);
-cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
+cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, int*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
                             const int32_t*, const void*, const float*, const float*, void*, float*, int*, int, int,
@@ -62,6 +64,7 @@ std::mutex g_mu;
 DevBuffers g_dev[kMaxDevices];
 thread_local int t_last_cuda_error = 0;
 thread_local cudaEvent_t t_phase_ev[3] = {nullptr, nullptr, nullptr};
+std::atomic<int> g_fail_allocs{0};  // gdn_debug_fail_allocations
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -89,14 +92,14 @@ size_t ws_bytes_for(int B, int T, int Hk, int Hv, int packed) {
   return 256 + table + ns * Hv * gdn::kWsPerSlotHead + ns * Hk * gdn::kWsNormPerSlotKHead;
 }
 
-int set_cuda_error(cudaError_t e, int code) {
-  t_last_cuda_error = (int)e;
-  return code;
-}
+using gdn::set_cuda_error;
 
-// Grow-only buffer for the current device.  Freeing synchronises the device.
+// Grow-only buffer for the current device.  Freeing synchronises the device.  An
+// injected failure (gdn_debug_fail_allocations) fails before anything is freed, so
+// the old buffer stays usable.
 int ensure(void*& ptr, size_t& have, size_t need) {
   if (need <= have) return GDN_OK;
+  if (gdn::take_injected_alloc_failure()) return set_cuda_error(cudaErrorMemoryAllocation, GDN_ERR_ALLOC);
   if (ptr != nullptr) {
     cudaError_t e = cudaFree(ptr);
     ptr = nullptr;
@@ -253,11 +256,11 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
   cudaError_t e = cudaSuccess;
   if (packed && table && (phases & 1)) {
-    e = gdn::launch_chunk_table(cu, B, T, chunk_off, st);
+    e = gdn::launch_chunk_table(cu, B, T, chunk_off, err, st);
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
-  cudaEvent_t ev[3] = {t_phase_ev[0], t_phase_ev[1], t_phase_ev[2]};
-  t_phase_ev[0] = t_phase_ev[1] = t_phase_ev[2] = nullptr;
+  cudaEvent_t ev[3];
+  gdn::take_phase_events(ev);
   if (ev[0] != nullptr && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (nslots > 0x7fffffffLL) return GDN_ERR_ARG;
   if (nslots > 0 && (phases & 1)) {
@@ -339,9 +342,36 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
 
 }  // namespace
 
+namespace gdn {
+
+int set_cuda_error(cudaError_t e, int code) {
+  t_last_cuda_error = (int)e;
+  return code;
+}
+
+void clear_cuda_error() { t_last_cuda_error = 0; }
+
+void take_phase_events(cudaEvent_t (&ev)[3]) {
+  for (int i = 0; i < 3; ++i) {
+    ev[i] = t_phase_ev[i];
+    t_phase_ev[i] = nullptr;
+  }
+}
+
+bool take_injected_alloc_failure() {
+  int n = g_fail_allocs.load();
+  while (n > 0 && !g_fail_allocs.compare_exchange_weak(n, n - 1)) {
+  }
+  return n > 0;
+}
+
+}  // namespace gdn
+
 extern "C" {
 
 int gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+int gdn_debug_fail_allocations(int count) { return g_fail_allocs.exchange(count < 0 ? 0 : count); }
 
 const char* gdn_strerror(int status) {
   switch (status) {
@@ -675,8 +705,8 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
   if (cu_seqlens != nullptr) {
     if ((rc = check(cudaMemcpyAsync(P(5), cu_seqlens, ncu, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK) return rc;
     int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + 256);
-    if ((rc = check(gdn::launch_chunk_table(reinterpret_cast<const int32_t*>(P(5)), B, T, chunk_off, d.h2d))) !=
-        GDN_OK)
+    if ((rc = check(gdn::launch_chunk_table(reinterpret_cast<const int32_t*>(P(5)), B, T, chunk_off,
+                                            static_cast<int*>(ws), d.h2d))) != GDN_OK)
       return rc;
   }
   if ((rc = check(cudaMemcpyAsync(P(3), g, ng, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK ||
@@ -733,18 +763,21 @@ int gdn_device_status(int* status) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_ARG;
-  void* ws = nullptr;
+  void* words[2] = {nullptr, gdn::static_scratch_address(dev)};  // the workspace's, the static array's
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    ws = g_dev[dev].ws;
+    words[0] = g_dev[dev].ws;
   }
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
-  if (ws == nullptr) return GDN_OK;
-  e = cudaMemcpy(status, ws, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
-  e = cudaMemset(ws, 0, sizeof(int));
-  if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+  for (void* w : words) {
+    if (w == nullptr) continue;
+    int bits = 0;
+    e = cudaMemcpy(&bits, w, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(w, 0, sizeof(int));
+    if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
+    *status |= bits;
+  }
   return GDN_OK;
 }
 

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace gdn {
 
 constexpr int kChunk = 64;  // tokens per chunk
@@ -105,19 +107,20 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// Raise a kernel's dynamic shared-memory limit once per device (a benign race if two
-// host threads do it at once).  Doing it once keeps later calls free of runtime
-// configuration calls, e.g. while a stream is being captured into a CUDA graph.
-// One flag set per kernel: the kernel itself is the template argument.
+// Raise a kernel's dynamic shared-memory limit once per device.  Doing it once keeps
+// later calls free of runtime configuration calls, e.g. while a stream is being captured
+// into a CUDA graph.  One flag set per kernel (the kernel is the template argument);
+// the flags are atomic, so concurrent first calls from several host threads at worst
+// both set the (same) attribute.
 template <auto kernel>
 inline cudaError_t set_smem_limit_once(int bytes) {
-  static bool done[64] = {};
+  static std::atomic<bool> done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
   return e;
 }
 

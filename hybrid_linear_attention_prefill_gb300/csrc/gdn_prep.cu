@@ -467,9 +467,12 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 }
 
 // Prefix sums of chunk counts for packed sequences: chunk_off[b] = sum over
-// b' < b of ceil(len_b' / 64), chunk_off[B] = total.  One CTA of 1024 threads.
+// b' < b of ceil(len_b' / 64), chunk_off[B] = total.  One CTA of 1024 threads.  It also
+// checks cu_seqlens (0 = cu[0] <= cu[1] <= ... <= cu[B] = T) and records status bit 8 when
+// the array is malformed; every kernel clamps the entries to [0, T] all the same.
 __global__ void __launch_bounds__(1024)
-gdn_chunk_table_kernel(const int32_t* __restrict__ cu, int B, int T, int32_t* __restrict__ chunk_off) {
+gdn_chunk_table_kernel(const int32_t* __restrict__ cu, int B, int T, int32_t* __restrict__ chunk_off,
+                       int* __restrict__ err) {
   __shared__ int wsum[32];
   __shared__ int carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -481,6 +484,8 @@ gdn_chunk_table_kernel(const int32_t* __restrict__ cu, int B, int T, int32_t* __
     if (b < B) {
       const SeqChunk s = seq_bounds(cu, b, T);
       nc = (s.len + kChunk - 1) / kChunk;
+      const int lo = cu[b], hi = cu[b + 1];
+      if (lo < 0 || hi < lo || hi > T || (b == 0 && lo != 0) || (b == B - 1 && hi != T)) atomicOr(err, 8);
     }
     int x = nc;
 #pragma unroll
@@ -567,8 +572,8 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_off, cudaStream_t st) {
-  gdn_chunk_table_kernel<<<1, 1024, 0, st>>>(cu, B, T, chunk_off);
+cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_off, int* err, cudaStream_t st) {
+  gdn_chunk_table_kernel<<<1, 1024, 0, st>>>(cu, B, T, chunk_off, err);
   return cudaGetLastError();
 }
 

@@ -22,10 +22,15 @@
 // Set-up.  The device address of the array is looked up once per device, with
 // that device current, by the first call made on it (cudaGetSymbolAddress).
 // Make that first call before capturing a stream into a CUDA graph.
+//
+// Status.  The kernels' status bits (a bounded wait that ran out, a malformed
+// cu_seqlens) go to the array's first word; gdn_device_status reads and clears it
+// together with the workspace's.
 #include <mutex>
 
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
+#include "gdn_internal.h"
 #include <climits>
 
 namespace gdn {
@@ -33,7 +38,8 @@ template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
                         void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, int,
                         cudaStream_t);
-cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, cudaStream_t);
+cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, int*, cudaStream_t);
+cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
                             const int32_t*, const void*, const float*, const float*, void*, float*, int*, int, int,
@@ -49,12 +55,35 @@ std::mutex g_static_mu;
 void* g_static_ptr[kMaxDev] = {};
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+// The array's device address on the current device, looked up on first use.
+cudaError_t static_base(int dev, void** base) {
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    g_static_ptr[dev] = p;
+  }
+  *base = g_static_ptr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
+
+namespace gdn {
+void* static_scratch_address(int dev) {
+  if (dev < 0 || dev >= kMaxDev) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  return g_static_ptr[dev];
+}
+}  // namespace gdn
 
 extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, const float* g,
                                   const float* beta, const int32_t* cu_seqlens, const float* init_state,
                                   void* out, float* final_state, int B, int T, int Hk, int Hv, int dk, int dv,
                                   void* stream) {
+  gdn::clear_cuda_error();
   const bool dims_ok = (dk == 32 || dk == 64 || dk == 128) && (dv == 32 || dv == 64 || dv == 128);
   if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || Hv % Hk != 0 || !dims_ok || Hv > 65535) return GDN_ERR_ARG;
   if ((long long)B * (dv / 32) > 0x7fffffffLL) return GDN_ERR_ARG;
@@ -79,19 +108,10 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return GDN_ERR_LAUNCH;
+  if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   if (dev < 0 || dev >= kMaxDev) return GDN_ERR_ARG;
   void* base = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_static_mu);
-    if (g_static_ptr[dev] == nullptr) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_static_scratch);
-      if (e != cudaSuccess || p == nullptr) return GDN_ERR_LAUNCH;
-      g_static_ptr[dev] = p;
-    }
-    base = g_static_ptr[dev];
-  }
+  if ((e = static_base(dev, &base)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(base);
@@ -100,22 +120,46 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   if (packed) {
-    e = gdn::launch_chunk_table(cu_seqlens, B, T, chunk_off, st);
-    if (e != cudaSuccess) return GDN_ERR_LAUNCH;
+    e = gdn::launch_chunk_table(cu_seqlens, B, T, chunk_off, err, st);
+    if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   }
+  // the gdn_set_phase_events hook: around the preparation and state-carry kernels
+  cudaEvent_t ev[3];
+  gdn::take_phase_events(ev);
+  if (ev[0] != nullptr && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   if (nslots > 0) {
     switch (dk) {
       case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
       case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
       default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
     }
-    if (e != cudaSuccess) return GDN_ERR_LAUNCH;
+    if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   }
+  if (ev[1] != nullptr && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   switch (dk) {
     case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
     case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
     default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
   }
-  if (e != cudaSuccess) return GDN_ERR_LAUNCH;
+  if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
+  if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
+  return GDN_OK;
+}
+
+// The bounded-wait self-test with the static array's status word as its target: the bit
+// it records is then read back by gdn_device_status, as a timed-out wait inside a
+// gdn_prefill_static call would be.  Synchronous; allocates nothing.
+extern "C" int gdn_selftest_static_wait_timeout(int max_polls) {
+  gdn::clear_cuda_error();
+  if (max_polls < 1) return GDN_ERR_ARG;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
+  if (dev < 0 || dev >= kMaxDev) return GDN_ERR_ARG;
+  void* base = nullptr;
+  if ((e = static_base(dev, &base)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
+  e = gdn::launch_wait_timeout_probe(max_polls, static_cast<int*>(base), nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   return GDN_OK;
 }

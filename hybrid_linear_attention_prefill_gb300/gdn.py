@@ -31,6 +31,7 @@ GDN_FLAG_ONE_LEVEL = 4
 GDN_STATUS_MMA_TIMEOUT = 1
 GDN_STATUS_LOAD_TIMEOUT = 2
 GDN_STATUS_PREP_LOAD_TIMEOUT = 4
+GDN_STATUS_BAD_CU_SEQLENS = 8
 
 
 def GDN_FLAG_SEGMENTS(n: int) -> int:
@@ -41,7 +42,8 @@ def GDN_FLAG_SEGMENTS(n: int) -> int:
 EXPORTED = ("gdn_abi_version", "gdn_strerror", "gdn_last_cuda_error", "gdn_prefill",
             "gdn_prefill_host", "gdn_prefill_static", "gdn_prefill_ws", "gdn_prefill_ex", "gdn_decode",
             "gdn_set_phase_events", "gdn_workspace_bytes", "gdn_scan_segments", "gdn_release_workspace",
-            "gdn_device_status", "gdn_selftest_wait_timeout")
+            "gdn_device_status", "gdn_selftest_wait_timeout", "gdn_selftest_static_wait_timeout",
+            "gdn_debug_fail_allocations")
 
 _lock = threading.Lock()
 _lib = None
@@ -102,6 +104,10 @@ def load(build_if_missing: bool = False):
         lib.gdn_device_status.restype = i
         lib.gdn_selftest_wait_timeout.argtypes = [i, ctypes.POINTER(ctypes.c_int)]
         lib.gdn_selftest_wait_timeout.restype = i
+        lib.gdn_selftest_static_wait_timeout.argtypes = [i]
+        lib.gdn_selftest_static_wait_timeout.restype = i
+        lib.gdn_debug_fail_allocations.argtypes = [i]
+        lib.gdn_debug_fail_allocations.restype = i
         lib.gdn_release_workspace.argtypes = []
         lib.gdn_release_workspace.restype = None
         _lib = lib
@@ -162,7 +168,7 @@ def gdn_set_phase_events(ev_begin, ev_mid, ev_end) -> None:
 
 
 def gdn_device_status():
-    """(status code, device status bits of the library workspace); clears the bits."""
+    """(status code, device status bits of the library workspace and the static array); clears them."""
     st = ctypes.c_int(0)
     rc = load().gdn_device_status(ctypes.byref(st))
     return rc, st.value
@@ -173,6 +179,16 @@ def gdn_selftest_wait_timeout(max_polls):
     st = ctypes.c_int(0)
     rc = load().gdn_selftest_wait_timeout(int(max_polls), ctypes.byref(st))
     return rc, st.value
+
+
+def gdn_selftest_static_wait_timeout(max_polls) -> int:
+    """A bounded wait made to run out, recording into gdn_prefill_static's status word."""
+    return load().gdn_selftest_static_wait_timeout(int(max_polls))
+
+
+def gdn_debug_fail_allocations(count) -> int:
+    """Make the library's next `count` device allocations fail; returns the pending count."""
+    return load().gdn_debug_fail_allocations(int(count))
 
 
 def gdn_release_workspace() -> None:

@@ -31,7 +31,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 2
+#define GDN_ABI_VERSION 3
 
 /* Status codes (0 = success, negative = error). */
 #define GDN_OK 0
@@ -80,8 +80,9 @@ int gdn_last_cuda_error(void);
  * T = Ttot, entries non-decreasing; zero-length sequences are allowed and return
  * their initial state.  The contents of cu_seqlens are not checked on the host
  * (that would need a synchronisation); out-of-range entries are clamped to
- * [0, T] on the device so no access leaves the buffers.  Value head h reads key
- * head h / (Hv / Hk).  dk and dv must each be 32, 64 or 128.
+ * [0, T] on the device so no access leaves the buffers, and a malformed array sets
+ * GDN_STATUS_BAD_CU_SEQLENS (see gdn_device_status).  Value head h reads key head
+ * h / (Hv / Hk).  dk and dv must each be 32, 64 or 128.
  *
  * Memory.  The library keeps a per-device, grow-only workspace (allocated on the
  * first call that needs more; about 16 KB per 64-token chunk and value head).
@@ -229,6 +230,9 @@ void gdn_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end);
  *   - The first call on each device looks the array's address up (with that device
  *     current); make that first call before capturing the stream into a CUDA graph.
  *   - Always the single-level path (no two-level scan).
+ *   - Status bits of its kernels go to the array's first word; gdn_device_status reads
+ *     and clears them with the workspace's.  gdn_set_phase_events applies as to
+ *     gdn_prefill, and gdn_last_cuda_error reports its launch errors.
  */
 int gdn_prefill_static(const void *q, const void *k, const void *v,
                        const float *g, const float *beta,
@@ -242,15 +246,18 @@ int gdn_prefill_static(const void *q, const void *k, const void *v,
  * TMA load) is bounded; a wait that runs out sets one of these bits in the first
  * word of the workspace, lets its copies and MMAs in flight land (bounded again),
  * frees its tensor memory and returns, so the context stays usable.  With
- * gdn_prefill_ws the word is the first 4 bytes of the caller's workspace.
+ * gdn_prefill_ws the word is the first 4 bytes of the caller's workspace; with
+ * gdn_prefill_static it is the first word of the fixed array.
  */
 #define GDN_STATUS_MMA_TIMEOUT 1       /* the state-carry kernel gave up waiting for an MMA phase */
 #define GDN_STATUS_LOAD_TIMEOUT 2      /* the state-carry kernel gave up waiting for a tile load */
 #define GDN_STATUS_PREP_LOAD_TIMEOUT 4 /* the preparation kernel gave up waiting for a tile load */
+#define GDN_STATUS_BAD_CU_SEQLENS 8    /* cu_seqlens was not 0 = cu[0] <= ... <= cu[B] = T (entries clamped) */
 
 /*
  * gdn_device_status -- synchronise the current device, return the status bits
- * accumulated in the library workspace since the last call (in *status) and
+ * accumulated since the last call (in *status: the OR of the library workspace's
+ * word and, once gdn_prefill_static has run on the device, the fixed array's) and
  * clear them.  Returns GDN_OK or GDN_ERR_LAUNCH.
  */
 int gdn_device_status(int *status);
@@ -263,6 +270,23 @@ int gdn_device_status(int *status);
  * fault.
  */
 int gdn_selftest_wait_timeout(int max_polls, int *status);
+
+/*
+ * gdn_selftest_static_wait_timeout -- the same bounded wait, but recording its bit in
+ * the status word of gdn_prefill_static's fixed array, where a wait that runs out
+ * inside that entry point would; gdn_device_status then reports it.  Synchronous;
+ * allocates nothing.  Returns GDN_OK, GDN_ERR_ARG (max_polls < 1) or GDN_ERR_LAUNCH.
+ */
+int gdn_selftest_static_wait_timeout(int max_polls);
+
+/*
+ * gdn_debug_fail_allocations -- test hook for failure handling: the next `count`
+ * device allocations the library would make (workspace, staging or scan buffers)
+ * fail as if cudaMalloc had run out of memory, so the call returns GDN_ERR_ALLOC
+ * before launching anything and keeps its previous buffers.  0 switches it off.
+ * Returns the count that was pending.  Needs no GPU.
+ */
+int gdn_debug_fail_allocations(int count);
 
 /* Segments per sequence that gdn_prefill_ex with these flags (gdn_prefill: flags = 0)
  * would use on the current device: 1 for the single-level path, P >= 2 for the

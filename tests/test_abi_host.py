@@ -129,3 +129,11 @@ def test_segment_flag_encoding():
     assert "#define GDN_FLAG_SEGMENTS(n) ((((unsigned)(n)) & 0xffu) << 8)" in hdr
     assert gdn.GDN_FLAG_SEGMENTS(3) == 3 << 8 and gdn.GDN_FLAG_SEGMENTS(255) == 0xFF00
     assert (gdn.GDN_FLAG_TWO_LEVEL, gdn.GDN_FLAG_ONE_LEVEL) == (2, 4)
+
+
+def test_allocation_failure_hook_counts_down(lib):
+    """gdn_debug_fail_allocations holds a count of upcoming failures and returns the one it replaces."""
+    assert gdn.gdn_debug_fail_allocations(2) == 0
+    assert gdn.gdn_debug_fail_allocations(5) == 2
+    assert gdn.gdn_debug_fail_allocations(-1) == 5   # negative: off
+    assert gdn.gdn_debug_fail_allocations(0) == 0

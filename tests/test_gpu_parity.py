@@ -270,8 +270,14 @@ def test_misaligned_device_pointer_rejected():
 
 
 def test_corrupt_cu_seqlens_stays_in_bounds():
-    """Out-of-range boundaries are clamped on the device: no fault, finite results."""
+    """Out-of-range boundaries are clamped on the device: no fault, finite results, and
+    the malformed array is reported as a status bit."""
+    from hybrid_linear_attention_prefill_gb300 import gdn
+
+    gdn.gdn_device_status()  # clear
     inp = make_gdn_inputs(lengths=[50, 50], Hk=1, Hv=1, dk=64, dv=64, seed=23)
     inp.cu_seqlens = np.array([0, 5000, 100], dtype=np.int32)
     o, s = run_gpu(inp)
     assert np.all(np.isfinite(s))
+    rc, bits = gdn.gdn_device_status()
+    assert rc == gdn.GDN_OK and bits == gdn.GDN_STATUS_BAD_CU_SEQLENS

@@ -8,7 +8,7 @@ the library-level form of that calling convention.
 import numpy as np
 import pytest
 
-from gpu_common import dev_inputs
+from gpu_common import OUT_TOL, STATE_TOL, dev_inputs, out_err, state_err
 from hybrid_linear_attention_prefill_gb300.inputs import make_gdn_inputs
 
 pytestmark = pytest.mark.gpu
@@ -81,6 +81,12 @@ def test_captured_graph_replays_with_new_inputs(gdn):
     gdn.check(gdn.gdn_prefill(*args(db), ref_o, ref_f, *dims))
     torch.cuda.synchronize()
     assert torch.equal(out, ref_o) and torch.equal(fin, ref_f)
+    # and the replayed graph's results stand against the float64 oracle on the new inputs
+    import oracle
+
+    o_ref, s_ref = oracle.prefill_inputs(b)
+    o, f = out.float().cpu().numpy(), fin.cpu().numpy()
+    assert out_err(o, o_ref) <= OUT_TOL and state_err(f, s_ref) <= STATE_TOL
     graph.replay()  # a second replay gives the same result
     torch.cuda.synchronize()
     assert torch.equal(out, ref_o) and torch.equal(fin, ref_f)
