@@ -24,6 +24,7 @@
 // operands are split into bf16 hi + lo parts (hi*hi + hi*lo + lo*hi, ~2^-16
 // relative).  Only non-positive exponents are ever taken (gamma_t - gamma_i,
 // i <= t), so nothing overflows however strong the decay.
+#include <atomic>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -34,9 +35,11 @@ namespace gdn {
 namespace {
 
 constexpr int kPrepThreads = 256;
+constexpr int kPrepCtasPerSm = 3;  // resident CTAs per SM: registers by the launch bounds, shared memory below
 constexpr int LDF = 68;  // fp32 row stride of 64-wide matrices
 constexpr int LDB = 72;  // bf16 row stride of 64-wide matrices
 constexpr int LDW = 36;  // fp32 row stride of the 32-wide merge buffer
+constexpr int LDE = 20;  // fp32 row stride of the 16-wide decay tables
 
 // acc (16 x 8 tile) += X[r0:r0+16, k0:k0+16] * Y[ky:ky+16, n0:n0+8] for fp32 X, Y in
 // shared memory, as three bf16 products of the hi / lo splits.
@@ -72,23 +75,24 @@ __device__ __forceinline__ void store_tile(float* D, int ldd, int r0, int n0, co
 
 template <int DK>
 struct PrepSmem {
-  // [union: K,Q tiles (TMA, 128 B swizzle) | A,Tm fp32] [G fp32 x2] [P bf16] [Tm bf16] [merge buffer]
-  // [inverse norms] [g, beta] [mbarriers]
+  // [union: K,Q tiles (TMA, 128 B swizzle) | A,Tm fp32] [P bf16] [Tm bf16 | decay tables]
+  // [merge buffer] [inverse norms] [column factors] [g, beta] [mbarriers]
+  // (the Grams stay in TMEM; the CTA fits three times on an SM)
   static constexpr int kKQBytes = 32768;
   static constexpr int kATBytes = 2 * kChunk * LDF * 4;
   static constexpr int kUnion = kKQBytes > kATBytes ? kKQBytes : kATBytes;
-  static constexpr int offG = kUnion;
-  static constexpr int offP = offG + 2 * kChunk * LDF * 4;
+  static constexpr int offP = kUnion;
   static constexpr int offTb = offP + kChunk * LDB * 2;
   static constexpr int offW = offTb + kChunk * LDB * 2;
   static constexpr int offRN = offW + 32 * LDW * 4;  // inverse norms of k rows, then q rows
-  static constexpr int offGB = offRN + 2 * kChunk * 4;   // [2 buffers][g 64 | beta 64] fp32
+  static constexpr int offCF = offRN + 2 * kChunk * 4;  // column factors [64]
+  static constexpr int offGB = offCF + kChunk * 4;       // [2 buffers][g 64 | beta 64] fp32
   static constexpr int offBar = offGB + 2 * 2 * kChunk * 4;
   static constexpr int bytes = offBar + 32 + 1024;  // 2 mbarriers + TMEM base; + slack for 1024-byte alignment
 };
 
 template <int DK>
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                 const float* __restrict__ g, const float* __restrict__ beta,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_off,
@@ -102,7 +106,6 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   unsigned char* KQ = smem;                    // [2][128][128 B], swizzled
   float* As = reinterpret_cast<float*>(smem);  // aliases K/Q after the Grams
   float* Tms = As + kChunk * LDF;
-  float* Gs = reinterpret_cast<float*>(smem + L::offG);  // [2][64][LDF]
   __nv_bfloat16* Ps = reinterpret_cast<__nv_bfloat16*>(smem + L::offP);
   __nv_bfloat16* Tmb = reinterpret_cast<__nv_bfloat16*>(smem + L::offTb);
   float* Wt = reinterpret_cast<float*>(smem + L::offW);  // [32][LDW]
@@ -111,6 +114,12 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   float* gbuf = reinterpret_cast<float*>(smem + L::offGB);
   float* rnk = reinterpret_cast<float*>(smem + L::offRN);  // 1/||k_t|| (1 without normalisation)
   float* rnq = rnk + kChunk;                                // 1/||q_t||
+  float* cfs = reinterpret_cast<float*>(smem + L::offCF);  // 1/||k_i|| 2^(gamma2_{i | 15} - gamma2_i)
+  // Decay tables of a value head, over the bf16 Tm (not in use while A and P are built):
+  // Es[b][r][c] = 2^(gamma2_{16b+r} - gamma2_{16b+c}) / ||k_{16b+c}|| for c <= r (else 0), and
+  // rfs[t][b] = 2^(gamma2_t - gamma2_{16b+15}) for the blocks b below t's own
+  float* Es = reinterpret_cast<float*>(smem + L::offTb);  // [4][16][LDE]
+  float* rfs = Es + 4 * 16 * LDE;                          // [64][4]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kKBlocks = DK > 64 ? 2 : 1;
@@ -202,7 +211,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Persistent CTAs (two per SM) walk the items with the grid's stride.  While one item is
+  // Persistent CTAs (as many per SM as fit) walk the items with the grid's stride.  While one item is
   // worked on, the next one's key and query tiles are brought into L2, so its tile copy
   // does not wait for DRAM.
   uint32_t ph = 0;  // phase of bar[0] and bar[1]: each completes once per item worked on
@@ -251,19 +260,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     if (!tc::mbar_wait(&bar[1], ph, 1u << 24)) atomicOr(err, 4);
     tc::fence_after();
-    // TMEM -> the fp32 Grams: warp w reads lanes 32 (w % 4) .. +31 (rows: 0..63 K, 64..127
-    // Q) and columns 32 (w / 4) .. +31
-    {
-      const int q4 = warp & 3, hf = warp >> 2;
-      float v[32];
-      tc::tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + 32 * hf, v);
-      float* dst = Gs + (q4 >> 1) * kChunk * LDF + (32 * (q4 & 1) + lane) * LDF + 32 * hf;
-#pragma unroll
-      for (int p = 0; p < 8; ++p)
-        *reinterpret_cast<float4*>(dst + 4 * p) = make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
-    }
-    tc::fence_before();
-    __syncthreads();  // Grams and norms visible; the tiles are dead from here on (A and Tm overwrite them)
+    __syncthreads();  // Grams done (they stay in TMEM) and norms visible; the tiles are dead from here on
 
 
     for (int gi = 0; gi < G; ++gi) {
@@ -287,55 +284,87 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       gl0 *= 1.4426950408889634f;  // log2(e)
       gl1 *= 1.4426950408889634f;
 
-      // ---- A (fp32) and P (bf16), 8 columns at a time, lower triangle only ----------
-      // Gamma[t][i] = 2^(gamma2_t - gamma2_i) with gamma2 = gamma log2(e): the exponent
-      // is never positive for i <= t.  A thread keeps one 8-column block (the CTA size is
-      // a multiple of 8), so its gamma and 1/||k|| columns are loaded once.
-      static_assert(kPrepThreads == 256, "two (row, column block) items per thread, rows tid / 8 and + 32");
-      const int c8 = (tid & 7) * 8;
-      float gcol[8], rcol[8];
+      // ---- the decay tables of this value head (every thread) ----------------------------
+      // Gamma[t][i] = 2^(gamma2_t - gamma2_i), i <= t, with every exponent <= 0: inside a
+      // 16 x 16 diagonal block from the table Es, below it as the product of a row factor
+      // (to the block's last column j0) and a column factor (from j0), both <= 1.
       {
+        auto g2of = [&](int x) {  // gamma2 of token x of the chunk (every lane takes part)
+          const float a = __shfl_sync(0xffffffffu, gl0, x & 31), c = __shfl_sync(0xffffffffu, gl1, x & 31);
+          return x < 32 ? a : c;
+        };
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {  // gamma of columns c8 .. c8 + 7 (tokens < 32 in gl0, the rest in gl1)
-          const float lo = __shfl_sync(0xffffffffu, gl0, (c8 + u) & 31);
-          const float hi = __shfl_sync(0xffffffffu, gl1, (c8 + u) & 31);
-          gcol[u] = c8 < 32 ? lo : hi;
+        for (int k = 0; k < 4; ++k) {
+          const int e = tid + kPrepThreads * k, bl = e >> 8, r = (e >> 4) & 15, c = e & 15;
+          const float gr = g2of(16 * bl + r), gc = g2of(16 * bl + c);
+          Es[(16 * bl + r) * LDE + c] = c <= r ? exp2f(gr - gc) * rnk[16 * bl + c] : 0.f;
         }
-        const float4 r0 = *reinterpret_cast<const float4*>(rnk + c8), r1 = *reinterpret_cast<const float4*>(rnk + c8 + 4);
-        rcol[0] = r0.x; rcol[1] = r0.y; rcol[2] = r0.z; rcol[3] = r0.w;
-        rcol[4] = r1.x; rcol[5] = r1.y; rcol[6] = r1.z; rcol[7] = r1.w;
+        {
+          const int t = tid >> 2, bl = tid & 3;
+          const float gt = g2of(t), gj = g2of(16 * bl + 15);
+          rfs[tid] = bl < (t >> 4) ? exp2f(gt - gj) : 0.f;
+        }
+        if (tid < kChunk) {
+          const float gi = g2of(tid), gj = g2of(tid | 15);
+          cfs[tid] = rnk[tid] * exp2f(gj - gi);
+        }
       }
-      // gamma of this thread's two rows, tid / 8 and tid / 8 + 32 (lane (tid / 8) % 32 of this warp)
-      const float grow0 = __shfl_sync(0xffffffffu, gl0, (tid >> 3) & 31);
-      const float grow1 = __shfl_sync(0xffffffffu, gl1, (tid >> 3) & 31);
-      for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
-        const int t = e >> 3;
-        float av[8], pv[8];
-        if (c8 <= t) {
-          const float gt = t < 32 ? grow0 : grow1, bt = gb[kChunk + t] * rnk[t], qt = rnq[t];
-          const float4 k0 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8);
-          const float4 k1 = *reinterpret_cast<const float4*>(Gs + t * LDF + c8 + 4);
-          const float4 q0 = *reinterpret_cast<const float4*>(Gs + kChunk * LDF + t * LDF + c8);
-          const float4 q1 = *reinterpret_cast<const float4*>(Gs + kChunk * LDF + t * LDF + c8 + 4);
-          const float gk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-          const float gq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      __syncthreads();
+
+      // ---- A (fp32) and P (bf16) straight from the Grams in TMEM ------------------------
+      // Warp w reads TMEM lanes 32 (w % 4) .. + 31 -- rows 0..63 of the Gram are K K^T (A),
+      // rows 64..127 Q K^T (P) -- and columns 32 (w / 4) .. + 31, 16 at a time.  A row's
+      // entries in a 16-column block are the Gram's times one factor per row and one per
+      // column: from Es in the row's own block (one row of it per lane), from the row and
+      // column factors below it.
+      {
+        const int q4 = warp & 3, hf = warp >> 2;
+        const bool isA = q4 < 2;
+        const int t = 32 * (q4 & 1) + lane;  // token of this row
+        const float sc = isA ? gb[kChunk + t] * rnk[t] : rnq[t];  // beta_t / ||k_t|| or 1 / ||q_t||
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int i = c8 + u;
-            const float dcy = i <= t ? exp2f(gt - gcol[u]) * rcol[u] : 0.f;
-            pv[u] = qt * dcy * gq[u];
-            av[u] = i < t ? bt * dcy * gk[u] : 0.f;
+        for (int sb = 0; sb < 2; ++sb) {
+          const int cb = 32 * hf + 16 * sb;
+          float o[16];
+          if (cb <= 32 * (q4 & 1) + 31) {  // warp-uniform: some row of the warp reaches column cb
+            float v[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + cb, v);
+            const bool own = t >= cb && t < cb + 16, below = t >= cb + 16;
+            const float* fp = own ? Es + t * LDE : cfs + cb;  // column factors of this row
+            const float s = own ? sc : below ? sc * rfs[4 * t + (cb >> 4)] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; u += 4) {
+              const float4 f = *reinterpret_cast<const float4*>(fp + u);
+              o[u] = s * f.x * v[u];
+              o[u + 1] = s * f.y * v[u + 1];
+              o[u + 2] = s * f.z * v[u + 2];
+              o[u + 3] = s * f.w * v[u + 3];
+            }
+            if (isA && own) {  // A is strictly lower triangular
+#pragma unroll
+              for (int u = 0; u < 16; ++u)
+                if (cb + u == t) o[u] = 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) o[u] = 0.f;
           }
-        } else {
+          if (isA) {
+            float* arow = As + t * LDF + cb;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) av[u] = pv[u] = 0.f;
+            for (int p = 0; p < 4; ++p)
+              *reinterpret_cast<float4*>(arow + 4 * p) = make_float4(o[4 * p], o[4 * p + 1], o[4 * p + 2], o[4 * p + 3]);
+          } else {
+            __nv_bfloat16* prow = Ps + t * LDB + cb;
+#pragma unroll
+            for (int p = 0; p < 2; ++p)
+              *reinterpret_cast<uint4*>(prow + 8 * p) =
+                  make_uint4(pack_bf16(o[8 * p], o[8 * p + 1]), pack_bf16(o[8 * p + 2], o[8 * p + 3]),
+                             pack_bf16(o[8 * p + 4], o[8 * p + 5]), pack_bf16(o[8 * p + 6], o[8 * p + 7]));
+          }
         }
-        *reinterpret_cast<float4*>(As + t * LDF + c8) = make_float4(av[0], av[1], av[2], av[3]);
-        *reinterpret_cast<float4*>(As + t * LDF + c8 + 4) = make_float4(av[4], av[5], av[6], av[7]);
-        *reinterpret_cast<uint4*>(Ps + t * LDB + c8) =
-            make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
-                       pack_bf16(pv[6], pv[7]));
       }
+      tc::fence_before();  // the TMEM reads are ordered before the next item's Gram product
       if (gi == 0) {  // the blocks of Tm above the diagonal stay zero for every value head
         for (int e = tid; e < kChunk * 16; e += kPrepThreads) {
           const int t = e >> 4, c4 = (e & 15) * 4;
@@ -554,7 +583,7 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   if (e != cudaSuccess) return e;
   if (cu == nullptr && (c_begin < 0 || c_count <= 0 || c_begin + c_count > nc_dense)) return cudaErrorInvalidValue;
   // items: key heads hk_base .. hk_base + hk_count - 1 of B sequences x c_count chunks (dense)
-  // or of every slot (packed).  With the device to itself: persistent CTAs, two per SM.  Beside
+  // or of every slot (packed).  With the device to itself: persistent CTAs, as many per SM as fit.  Beside
   // other kernels (the host entry's pipelines) a CTA per item, so that the hardware spreads the
   // items over whatever SMs come free.
   const long long n_items = (cu == nullptr ? (long long)B * c_count : (long long)nslots) * hk_count;
@@ -564,7 +593,19 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  const long long grid = persistent && n_items > 2LL * sms ? 2LL * sms : n_items;
+  // kPrepCtasPerSm CTAs on every SM: the launch bounds keep the registers within an SM's
+  // share, and all of the unified L1 / shared memory goes to shared memory (the driver's
+  // default split fits fewer)
+  static_assert(kPrepCtasPerSm * (L::bytes + 1024) <= 228 * 1024, "the CTAs of an SM do not fit in shared memory");
+  static std::atomic<bool> carved[64] = {};
+  if (dev < 0 || dev >= 64 || !carved[dev].load(std::memory_order_acquire)) {
+    if ((e = cudaFuncSetAttribute(gdn_prep_kernel<DK>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+    if (dev >= 0 && dev < 64) carved[dev].store(true, std::memory_order_release);
+  }
+  const long long resident = (long long)sms * kPrepCtasPerSm;
+  const long long grid = persistent && n_items > resident ? resident : n_items;
   gdn_prep_kernel<DK><<<(unsigned)grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
                                                            static_cast<__nv_bfloat16*>(ws), ws_rn, err, B, T, Hk, Hv,
                                                            nc_dense, norm_qk, hk_base, hk_count, c_begin,
