@@ -215,6 +215,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   // worked on, the next one's key and query tiles are brought into L2, so its tile copy
   // does not wait for DRAM.
   uint32_t ph = 0;  // phase of bar[0] and bar[1]: each completes once per item worked on
+  int ahead = -1;   // (thread 0) the item whose tiles went out while the one before it was worked on
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     Item cur;
     if (!locate(item, cur)) continue;  // the same for every thread of the CTA
@@ -223,7 +224,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     // the loads of this item (the first item's went out before the set-up barrier)
     if (item != (int)blockIdx.x) {
       load_gb(cur, 0, 0);
-      if (tid == 0) load_tiles(item, cur);
+      if (tid == 0 && item != ahead) load_tiles(item, cur);
     }
     if (!tc::mbar_wait(&bar[0], ph, 1u << 24)) atomicOr(err, 4);
     // rows t >= n belong to the next sequence (or are past the end): clear them
@@ -289,23 +290,25 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       // 16 x 16 diagonal block from the table Es, below it as the product of a row factor
       // (to the block's last column j0) and a column factor (from j0), both <= 1.
       {
-        auto g2of = [&](int x) {  // gamma2 of token x of the chunk (every lane takes part)
-          const float a = __shfl_sync(0xffffffffu, gl0, x & 31), c = __shfl_sync(0xffffffffu, gl1, x & 31);
-          return x < 32 ? a : c;
-        };
+        // gamma2 of token x: lane x % 32 holds it in gl0 (x < 32) or gl1; where the half is
+        // the same for the whole warp, one shuffle fetches it
+        auto g2u = [&](bool upper, int x) { return __shfl_sync(0xffffffffu, upper ? gl1 : gl0, x & 31); };
+        static_assert(kPrepThreads == 256, "one table row block per 256 entries");
+        const int r = (tid >> 4) & 15, c = tid & 15;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int e = tid + kPrepThreads * k, bl = e >> 8, r = (e >> 4) & 15, c = e & 15;
-          const float gr = g2of(16 * bl + r), gc = g2of(16 * bl + c);
+        for (int bl = 0; bl < 4; ++bl) {  // Es[bl][r][c], the block's half of the tokens known at compile time
+          const float gr = g2u(bl >= 2, 16 * bl + r), gc = g2u(bl >= 2, 16 * bl + c);
           Es[(16 * bl + r) * LDE + c] = c <= r ? exp2f(gr - gc) * rnk[16 * bl + c] : 0.f;
         }
         {
-          const int t = tid >> 2, bl = tid & 3;
-          const float gt = g2of(t), gj = g2of(16 * bl + 15);
-          rfs[tid] = bl < (t >> 4) ? exp2f(gt - gj) : 0.f;
+          const int t = tid >> 2, bl = tid & 3;  // t < 32 for warps 0..3
+          const float gt = g2u(tid >= 128, t);
+          const float j0 = __shfl_sync(0xffffffffu, gl0, (16 * bl + 15) & 31);
+          const float j1 = __shfl_sync(0xffffffffu, gl1, (16 * bl + 15) & 31);
+          rfs[tid] = bl < (t >> 4) ? exp2f(gt - (bl < 2 ? j0 : j1)) : 0.f;
         }
-        if (tid < kChunk) {
-          const float gi = g2of(tid), gj = g2of(tid | 15);
+        if (tid < kChunk) {  // warps 0 and 1: tokens tid
+          const float gi = tid < 32 ? gl0 : gl1, gj = g2u(tid >= 32, tid | 15);
           cfs[tid] = rnk[tid] * exp2f(gj - gi);
         }
       }
@@ -442,7 +445,18 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         *reinterpret_cast<uint4*>(Tmb + r * LDB + 8 * p) = v;
         *reinterpret_cast<uint4*>(wsT + r * kChunk + 8 * p) = v;
       }
+      if (gi == G - 1) tc::fence_proxy_async();  // fp32 A and Tm are dead: the next tiles may land over them
       __syncthreads();
+      if (gi == G - 1 && tid == 0) {  // the CTA's next item's tile copy overlaps PT and the stores
+        for (int nx = item + (int)gridDim.x; nx < n_items; nx += gridDim.x) {
+          Item it;
+          if (locate(nx, it)) {
+            load_tiles(nx, it);
+            ahead = nx;
+            break;
+          }
+        }
+      }
 
       // ---- PT = P Tm (lower triangular); warp w: rows 16 (w/2).., column pairs ---
       {
