@@ -20,11 +20,11 @@ template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
                         void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, int,
                         cudaStream_t);
-cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, int*, cudaStream_t);
+cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, int32_t*, int*, cudaStream_t);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
-                            const int32_t*, const void*, const float*, const float*, void*, float*, int*, int, int,
-                            int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
+                            const int32_t*, const int32_t*, const void*, const float*, const float*, void*, float*,
+                            int*, int, int, int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int32_t*, int, int, int, int, int, int, int,
                              cudaStream_t);
@@ -84,10 +84,10 @@ long long num_slots(int B, int T, int packed) {
   return (long long)(T + gdn::kChunk - 1) / gdn::kChunk + B;
 }
 
-// Workspace: [256 B status words][chunk table, B + 1 int32, padded to 256 B]
+// Workspace: [256 B status words][chunk table and dispatch order (chunk_table_bytes)]
 //            [Tm/PT tiles per (slot, value head)][inverse q/k norms per (slot, key head)]
 size_t ws_bytes_for(int B, int T, int Hk, int Hv, int packed) {
-  const size_t table = align_up(sizeof(int32_t) * ((size_t)B + 1), 256);
+  const size_t table = gdn::chunk_table_bytes(B);
   const size_t ns = (size_t)num_slots(B, T, packed);
   return 256 + table + ns * Hv * gdn::kWsPerSlotHead + ns * Hk * gdn::kWsNormPerSlotKHead;
 }
@@ -213,8 +213,9 @@ cudaError_t chain(const void* q, const void* k, const void* v, const float* g, c
                   const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* ws_rn,
                   const float* init, void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV,
                   int nc_dense, long long nslots, int norm_qk, cudaStream_t st) {
-  return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv,
-                                  DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, st);
+  // the two-level scan's runs are packed views of segments: dispatched in their own order
+  return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, nullptr, tiles, ws_rn, init, out, fin, err, B, T,
+                                  Hk, Hv, DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, st);
 }
 
 cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -243,7 +244,8 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   const int packed = cu != nullptr;
   int* err = static_cast<int*>(ws);
   int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + 256);
-  void* tiles = static_cast<unsigned char*>(ws) + 256 + align_up(sizeof(int32_t) * ((size_t)B + 1), 256);
+  int32_t* order = packed ? chunk_off + B + 1 : nullptr;  // packed: state carries longest first
+  void* tiles = static_cast<unsigned char*>(ws) + 256 + gdn::chunk_table_bytes(B);
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   const long long nslots = num_slots(B, T, packed);
   if (c1 < 0) c1 = nc_dense;
@@ -256,7 +258,7 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
   cudaError_t e = cudaSuccess;
   if (packed && table && (phases & 1)) {
-    e = gdn::launch_chunk_table(cu, B, T, chunk_off, err, st);
+    e = gdn::launch_chunk_table(cu, B, T, chunk_off, order, err, st);
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
   cudaEvent_t ev[3];
@@ -331,9 +333,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     return GDN_OK;
   }
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
   }
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
@@ -706,7 +708,7 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
     if ((rc = check(cudaMemcpyAsync(P(5), cu_seqlens, ncu, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK) return rc;
     int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) + 256);
     if ((rc = check(gdn::launch_chunk_table(reinterpret_cast<const int32_t*>(P(5)), B, T, chunk_off,
-                                            static_cast<int*>(ws), d.h2d))) != GDN_OK)
+                                            chunk_off + B + 1, static_cast<int*>(ws), d.h2d))) != GDN_OK)
       return rc;
   }
   if ((rc = check(cudaMemcpyAsync(P(3), g, ng, cudaMemcpyHostToDevice, d.h2d))) != GDN_OK ||

@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
                     const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu,
-                    const int32_t* __restrict__ chunk_off, const float* __restrict__ ws_rn, const float* init,
+                    const int32_t* __restrict__ chunk_off, const int32_t* __restrict__ order,
+                    const float* __restrict__ ws_rn, const float* init,
                     __nv_bfloat16* __restrict__ out,
                     float* fin, int* __restrict__ err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
                     long long nslots, int h_base, int c_begin, int c_end) {
@@ -159,9 +160,21 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int cg = (warp >> 2) & 1;  // column group: state columns 16 cg .. 16 cg + 15
   const int row = 32 * q4 + lane;
   const int ntiles = DV / kDVT;
-  const int b = blockIdx.x / ntiles;
-  const int dv0 = (blockIdx.x - b * ntiles) * kDVT;
-  const int h = h_base + (int)blockIdx.y;
+  // CTA (x, y) = (sequence b x slices + slice, head).  With a dispatch order (packed batches),
+  // the CTA's position in dispatch order walks the sequences most chunks first, and every
+  // head and slice of one sequence before the next, so that the long chains start first.
+  int bx = (int)blockIdx.x, hy = (int)blockIdx.y;
+  if (order != nullptr) {
+    const long long pos = (long long)blockIdx.y * gridDim.x + blockIdx.x;
+    const int per = (int)gridDim.y * ntiles;  // CTAs of one sequence
+    const int r = (int)(pos / per), rem = (int)(pos - (long long)r * per);
+    const int ob = order[r];
+    hy = rem / ntiles;
+    bx = (ob >= 0 && ob < B ? ob : r) * ntiles + rem % ntiles;
+  }
+  const int b = bx / ntiles;
+  const int dv0 = (bx - b * ntiles) * kDVT;
+  const int h = h_base + hy;
   const int hk = h / (Hv / Hk);
   const float scale = rsqrtf((float)DK);
   constexpr int kP1 = DK / 16 < kParts ? DK / 16 : kParts;  // partials used by phase 1
@@ -480,8 +493,8 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 template <int DK>
 cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                            const int32_t* cu, const int32_t* chunk_off, const void* ws, const float* ws_rn,
-                            const float* init,
+                            const int32_t* cu, const int32_t* chunk_off, const int32_t* order, const void* ws,
+                            const float* ws_rn, const float* init,
                             void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
                             long long nslots, int norm_qk, int h_base, int h_count, int c_begin, int c_end,
                             cudaStream_t st) {
@@ -514,7 +527,7 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
                           : set_smem_limit_once<gdn_chain_tc_kernel<DK, false>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)B * (DV / kDVT), h_count);  // value heads h_base .. h_base + h_count - 1
-  kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, ws_rn, init,
+  kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, order, ws_rn, init,
                                               static_cast<__nv_bfloat16*>(out), fin, err, B, T, Hk, Hv, DV,
                                               nc_dense, nslots, h_base, c_begin, c_end);
   return cudaGetLastError();
@@ -522,8 +535,8 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
 
 #define GDN_INST_CHAIN_TC(DK)                                                                                \
   template cudaError_t launch_chain_tc<DK>(const void*, const void*, const void*, const float*, const float*, \
-                                           const int32_t*, const int32_t*, const void*, const float*,         \
-                                           const float*, void*,                                               \
+                                           const int32_t*, const int32_t*, const int32_t*, const void*,       \
+                                           const float*, const float*, void*,                                 \
                                            float*, int*, int, int, int, int, int, int, long long, int, int,   \
                                            int, int, int, cudaStream_t);
 GDN_INST_CHAIN_TC(32)

@@ -21,6 +21,10 @@ constexpr size_t kWsPerSlotHead = 2 * kWsTileElems * 2;  // bytes (Tm + PT)
 // k rows then q rows (fp32, 64 + 64), written by the preparation kernel when q and k
 // are normalised in-kernel.
 constexpr size_t kWsNormPerSlotKHead = 2 * kChunk * 4;  // bytes
+// Before the tiles (after 256 bytes of status words): the packed chunk table, B + 1 int32
+// chunk offsets, then the B sequences in the order their state carries are dispatched
+// (most chunks first), padded to 256 bytes.
+inline size_t chunk_table_bytes(int B) { return (sizeof(int32_t) * (2 * (size_t)B + 1) + 255) / 256 * 256; }
 
 struct SeqChunk {
   long long bos;  // first token of the sequence

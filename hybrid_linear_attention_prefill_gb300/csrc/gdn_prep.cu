@@ -512,12 +512,16 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // Prefix sums of chunk counts for packed sequences: chunk_off[b] = sum over
 // b' < b of ceil(len_b' / 64), chunk_off[B] = total.  One CTA of 1024 threads.  It also
 // checks cu_seqlens (0 = cu[0] <= cu[1] <= ... <= cu[B] = T) and records status bit 8 when
-// the array is malformed; every kernel clamps the entries to [0, T] all the same.
+// the array is malformed; every kernel clamps the entries to [0, T] all the same.  With
+// `order`, it also writes the sequences most chunks first (chunk counts above 1022 share
+// one bucket): the state carry dispatches its CTAs in that order, so that the longest chains
+// do not start in the last wave.
 __global__ void __launch_bounds__(1024)
 gdn_chunk_table_kernel(const int32_t* __restrict__ cu, int B, int T, int32_t* __restrict__ chunk_off,
-                       int* __restrict__ err) {
+                       int32_t* __restrict__ order, int* __restrict__ err) {
   __shared__ int wsum[32];
   __shared__ int carry;
+  __shared__ int bucket[1024];  // sequences per chunk count, most chunks first: key 1023 - min(chunks, 1023)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) carry = 0;
   __syncthreads();
@@ -555,6 +559,43 @@ gdn_chunk_table_kernel(const int32_t* __restrict__ cu, int B, int T, int32_t* __
     __syncthreads();
   }
   if (tid == 0) chunk_off[B] = carry;
+
+  // ---- dispatch order of the state carries: a counting sort on the chunk counts, most first
+  // (sequences with the same count in any order; every sequence appears once) ----
+  if (order == nullptr) return;
+  auto key = [&](int b) {
+    const int nc = (seq_bounds(cu, b, T).len + kChunk - 1) / kChunk;
+    return 1023 - (nc < 1023 ? nc : 1023);
+  };
+  bucket[tid] = 0;
+  __syncthreads();
+  for (int b = tid; b < B; b += 1024) atomicAdd(&bucket[key(b)], 1);
+  __syncthreads();
+  // exclusive prefix sum of the 1024 bucket sizes (one per thread)
+  {
+    const int n = bucket[tid];
+    int x = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      wsum[lane] = w;
+    }
+    __syncthreads();
+    bucket[tid] = (warp ? wsum[warp - 1] : 0) + x - n;  // first position of the bucket
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += 1024) order[atomicAdd(&bucket[key(b)], 1)] = b;
 }
 
 // ---- launchers -----------------------------------------------------------------
@@ -627,8 +668,9 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_off, int* err, cudaStream_t st) {
-  gdn_chunk_table_kernel<<<1, 1024, 0, st>>>(cu, B, T, chunk_off, err);
+cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_off, int32_t* order, int* err,
+                               cudaStream_t st) {
+  gdn_chunk_table_kernel<<<1, 1024, 0, st>>>(cu, B, T, chunk_off, order, err);
   return cudaGetLastError();
 }
 

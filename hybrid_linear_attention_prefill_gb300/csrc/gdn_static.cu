@@ -38,12 +38,12 @@ template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
                         void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, int,
                         cudaStream_t);
-cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, int*, cudaStream_t);
+cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, int32_t*, int*, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
-                            const int32_t*, const void*, const float*, const float*, void*, float*, int*, int, int,
-                            int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
+                            const int32_t*, const int32_t*, const void*, const float*, const float*, void*, float*,
+                            int*, int, int, int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
 }  // namespace gdn
 
 namespace {
@@ -97,11 +97,11 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
     if (p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return GDN_ERR_ALIGN;
   if (ntok == 0 && final_state == nullptr) return GDN_OK;
 
-  // scratch layout: [256 B status words][chunk table, B + 1 int32, padded to 256 B][Tm/PT tiles]
+  // scratch layout: [256 B status words][chunk table and dispatch order][Tm/PT tiles]
   //                 [inverse q/k norms per (slot, key head)]
   const long long nslots = packed ? (long long)(T + gdn::kChunk - 1) / gdn::kChunk + B
                                   : (long long)B * ((T + gdn::kChunk - 1) / gdn::kChunk);
-  const size_t table = round256(sizeof(int32_t) * ((size_t)B + 1));
+  const size_t table = gdn::chunk_table_bytes(B);
   const size_t need = 256 + table + (size_t)nslots * Hv * gdn::kWsPerSlotHead +
                       (size_t)nslots * Hk * gdn::kWsNormPerSlotKHead;
   if (need > (size_t)GDN_STATIC_SCRATCH_BYTES || nslots > 0x7fffffffLL) return GDN_ERR_SCRATCH;
@@ -116,11 +116,12 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(base);
   int32_t* chunk_off = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + 256);
+  int32_t* order = packed ? chunk_off + B + 1 : nullptr;  // packed: state carries longest first
   void* tiles = static_cast<unsigned char*>(base) + 256 + table;
   float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   if (packed) {
-    e = gdn::launch_chunk_table(cu_seqlens, B, T, chunk_off, err, st);
+    e = gdn::launch_chunk_table(cu_seqlens, B, T, chunk_off, order, err, st);
     if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   }
   // the gdn_set_phase_events hook: around the preparation and state-carry kernels
@@ -137,9 +138,9 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   }
   if (ev[1] != nullptr && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, st); break;
   }
   if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);

@@ -171,8 +171,8 @@ def make_gdn_inputs(
     )
 
 
-# The five workloads: shapes and distributions of independent candidate
-# prompts (default limit 4,096 tokens, maximum 16,384).
+# The five workloads (plus a smaller packed batch for profiling): shapes and distributions
+# of independent candidate prompts (default limit 4,096 tokens, maximum 16,384).
 WORKLOADS = {
     "tiny_t64_d32": dict(B=1, T=64, Hk=1, Hv=1, dk=32, dv=32),
     "t1024_h16": dict(B=1, T=1024, Hk=16, Hv=16, dk=128, dv=128),
@@ -184,6 +184,9 @@ WORKLOADS = {
     # chunk-sequential carry alone would leave most SMs idle
     "t16384_hk4_hv4_carry": dict(B=1, T=16384, Hk=4, Hv=4, dk=128, dv=128,
                                  g_scale=0.1, init_std=0.02),
+    # the packed batch's length mix at a quarter of its candidates: small enough for a
+    # many-pass profiler capture of one launch, larger than L2
+    "varlen8_hk16_hv32": dict(lengths=("uniform", 8, 200, 4096), Hk=16, Hv=32, dk=128, dv=128),
 }
 
 HEADLINE = "t4096_hk16_hv32"

@@ -108,6 +108,21 @@ def test_packed_with_empty_sequences():
         assert np.array_equal(s[b], inp.init[b])
 
 
+def test_packed_dispatch_order_many_and_long_sequences():
+    """The packed state carries run longest first through a device-built order (a counting sort
+    on chunk counts, counts above 1022 sharing one bucket).  More than 1,024 sequences take the
+    sort's loops more than once; one sequence of 1,100 chunks lands in the shared bucket; empty
+    sequences sort last.  Every sequence is still carried exactly once, from its own state."""
+    rng = np.random.default_rng(90)
+    lengths = [int(x) for x in rng.integers(0, 140, 1500)]
+    lengths[700] = 1100 * 64 - 5
+    lengths[3] = 0
+    inp = make_gdn_inputs(lengths=lengths, Hk=1, Hv=2, dk=32, dv=32, seed=91, init_std=0.1)
+    o, s = check_full(inp)
+    for b in [i for i, n in enumerate(lengths) if n == 0][:20]:
+        assert np.array_equal(s[b], inp.init[b])
+
+
 def test_slow_decay_many_chunks_with_carry():
     """g ~ -0.01 softplus keeps the initial state and early chunks alive across 16 chunks."""
     check_full(make_gdn_inputs(B=1, T=1000, Hk=2, Hv=4, dk=128, dv=128, seed=11, g_scale=0.01,
