@@ -251,7 +251,7 @@ int gdn_prefill_static(const void *q, const void *k, const void *v,
  */
 #define GDN_STATUS_MMA_TIMEOUT 1       /* the state-carry kernel gave up waiting for an MMA phase */
 #define GDN_STATUS_LOAD_TIMEOUT 2      /* the state-carry kernel gave up waiting for a tile load */
-#define GDN_STATUS_PREP_LOAD_TIMEOUT 4 /* the preparation kernel gave up waiting for a tile load */
+#define GDN_STATUS_PREP_LOAD_TIMEOUT 4 /* the preparation kernel gave up waiting (tile load or Gram product) */
 #define GDN_STATUS_BAD_CU_SEQLENS 8    /* cu_seqlens was not 0 = cu[0] <= ... <= cu[B] = T (entries clamped) */
 
 /*
