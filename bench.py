@@ -383,7 +383,8 @@ def run_gpu_arm(args):
             "config": workload_config(args, inp, world),
             "roofline": roofline, "path_roofline": path_roof,
             "kernels_us": {k: round(v * 1e3, 2) for k, v in kernels.items()},
-            "ms_per_step_min": min(step_ms), "wall_s": round(wall, 3),
+            "ms_per_step_min": min(step_ms), "ms_per_step_median": statistics.median(step_ms),
+            "wall_s": round(wall, 3),
             "cpu_baseline": cpu, "e2e": e2e,
             # prep + state carry (+ chunk table when packed); the two-level scan adds the
             # segment set-up, a second pass-A carry, the combine and pass C
@@ -426,7 +427,7 @@ def measure_e2e(inp, gdn, torch, stream, steps):
 # measurements of the adjacent entry points (one JSON line each, device timing)
 # ---------------------------------------------------------------------------
 def _timed_steps(torch, stream, flush, step, warmup, K):
-    """Mean and min milliseconds of `step` over K calls, L2 flushed before each."""
+    """Mean, min and median milliseconds of `step` over K calls, L2 flushed before each."""
     for _ in range(warmup):
         flush.zero_()
         step()
@@ -439,7 +440,7 @@ def _timed_steps(torch, stream, flush, step, warmup, K):
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
-    return statistics.mean(ms), min(ms)
+    return statistics.mean(ms), min(ms), statistics.median(ms)
 
 
 def run_extra_arm(args):
@@ -471,13 +472,14 @@ def run_extra_arm(args):
                                      B, Hk, Hv, dk, dv, stream))
 
         sampler.start()
-        ms, ms_min = _timed_steps(torch, stream, flush, step, args.warmup, args.steps)
+        ms, ms_min, ms_med = _timed_steps(torch, stream, flush, step, args.warmup, args.steps)
         clocks = sampler.stop()
         nbytes = 2 * B * Hv * dv * dk * 4 + B * (2 * Hk * dk + 2 * Hv * dv) * 2 + 2 * B * Hv * 4
         achieved = nbytes / (ms * 1e-3) / 1e9
         line = {"metric": "GDN decode tokens/s (one token per sequence, state updated in place)",
                 "value": B / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_min": ms_min, "higher_is_better": True,
+                "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_min": ms_min, "ms_per_step_median": ms_med,
+                "higher_is_better": True,
                 "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": f"decode_b{B}_hk{Hk}_hv{Hv}", "B": B, "Hk": Hk, "Hv": Hv, "dk": dk,
                            "dv": dv, "state_bytes": B * Hv * dv * dk * 4,
@@ -515,12 +517,13 @@ def run_extra_arm(args):
         def step():
             graph.replay()
     sampler.start()
-    ms, ms_min = _timed_steps(torch, stream, flush, step, args.warmup, args.steps)
+    ms, ms_min, ms_med = _timed_steps(torch, stream, flush, step, args.warmup, args.steps)
     clocks = sampler.stop()
     alg = algorithmic(inp)
     t_hbm = alg["total"] / (peaks["hbm"] * 1e9)
     line = {"metric": METRIC, "value": Tt / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_min": ms_min, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_min": ms_min, "ms_per_step_median": ms_med,
+                "higher_is_better": True,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "mode": mode, "B": B, "T": inp.T, "Hk": inp.Hk, "Hv": inp.Hv,
                        "dk": inp.dk, "dv": inp.dv, "l2": "flushed between timed steps (256 MB write)"},
