@@ -35,7 +35,7 @@ namespace gdn {
 namespace {
 
 constexpr int kPrepThreads = 256;
-constexpr int kPrepCtasPerSm = 3;  // resident CTAs per SM: registers by the launch bounds, shared memory below
+constexpr int kPrepCtasPerSm = 4;  // resident CTAs per SM: registers by the launch bounds, shared memory below
 constexpr int LDF = 68;  // fp32 row stride of 64-wide matrices
 constexpr int LDB = 72;  // bf16 row stride of 64-wide matrices
 constexpr int LDW = 36;  // fp32 row stride of the 32-wide merge buffer
@@ -75,16 +75,20 @@ __device__ __forceinline__ void store_tile(float* D, int ldd, int r0, int n0, co
 
 template <int DK>
 struct PrepSmem {
-  // [union: K,Q tiles (TMA, 128 B swizzle) | A,Tm fp32] [P bf16] [Tm bf16 | decay tables]
-  // [merge buffer] [inverse norms] [column factors] [g, beta] [mbarriers]
-  // (the Grams stay in TMEM; the CTA fits three times on an SM)
+  // [union: K,Q tiles (TMA, 128 B swizzle) | A,Tm fp32] [P bf16] [Tm bf16 | decay tables |
+  // merge buffer] [inverse norms] [column factors] [g, beta] [mbarriers]
+  // (the Grams stay in TMEM; the CTA fits four times on an SM).  Within a value head the decay
+  // tables live until A and P are built, the merge buffer through the 16 -> 32 -> 64 merges and
+  // the bf16 Tm from then on, so the three share one region.
   static constexpr int kKQBytes = 32768;
   static constexpr int kATBytes = 2 * kChunk * LDF * 4;
   static constexpr int kUnion = kKQBytes > kATBytes ? kKQBytes : kATBytes;
   static constexpr int offP = kUnion;
   static constexpr int offTb = offP + kChunk * LDB * 2;
-  static constexpr int offW = offTb + kChunk * LDB * 2;
-  static constexpr int offRN = offW + 32 * LDW * 4;  // inverse norms of k rows, then q rows
+  static constexpr int offW = offTb;                   // the merge buffer, over the bf16 Tm
+  static constexpr int offRN = offTb + kChunk * LDB * 2;  // inverse norms of k rows, then q rows
+  static_assert(32 * LDW * 4 <= kChunk * LDB * 2, "the merge buffer fits over the bf16 Tm");
+  static_assert(4 * 16 * LDE * 4 + kChunk * 4 * 4 <= kChunk * LDB * 2, "the decay tables fit over the bf16 Tm");
   static constexpr int offCF = offRN + 2 * kChunk * 4;  // column factors [64]
   static constexpr int offGB = offCF + kChunk * 4;       // [2 buffers][g 64 | beta 64] fp32
   static constexpr int offBar = offGB + 2 * 2 * kChunk * 4;
