@@ -24,7 +24,8 @@ cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, int32_t*, int
 template <int DK>
 cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
                             const int32_t*, const int32_t*, const void*, const float*, const float*, void*, float*,
-                            int*, int, int, int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
+                            int*, int, int, int, int, int, int, long long, int, int, int, int, int, int,
+                            cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int32_t*, int, int, int, int, int, int, int,
                              cudaStream_t);
@@ -215,7 +216,7 @@ cudaError_t chain(const void* q, const void* k, const void* v, const float* g, c
                   int nc_dense, long long nslots, int norm_qk, cudaStream_t st) {
   // the two-level scan's runs are packed views of segments: dispatched in their own order
   return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, nullptr, tiles, ws_rn, init, out, fin, err, B, T,
-                                  Hk, Hv, DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, st);
+                                  Hk, Hv, DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, 0, st);
 }
 
 cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -234,10 +235,12 @@ cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const 
 int launch_all(const void* q, const void* k, const void* v, const float* g, const float* beta,
                const int32_t* cu, const float* init, void* out, float* fin, int B, int T, int Hk, int Hv,
                int dk, int dv, cudaStream_t st, void* ws, int norm_qk = 0, const ScanPlan* plan = nullptr,
-               int h0 = 0, int h1 = -1, bool table = true, int c0 = 0, int c1 = -1, int phases = 3) {
+               int h0 = 0, int h1 = -1, bool table = true, int c0 = 0, int c1 = -1, int phases = 3,
+               int slice = 0) {
   // [h0, h1): value heads; [c0, c1): the window of each dense sequence's chunks (-1: all).
   // A window's launches carry the state from `init` to `fin` over its chunks only.
   // phases: bit 0 the preparation kernel (and the packed chunk table), bit 1 the state carry.
+  // slice: state rows per state-carry CTA (32, 64; 0 = the library's choice).
   if (h1 < 0) h1 = Hv;
   const int G = Hv / Hk;
   const int hk0 = h0 / G, nhk = (h1 - h0) / G;
@@ -333,9 +336,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     return GDN_OK;
   }
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, st); break;
+    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, slice, st); break;
+    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, slice, st); break;
+    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, slice, st); break;
   }
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
@@ -396,7 +399,8 @@ void gdn_set_phase_events(void* ev_begin, void* ev_mid, void* ev_end) {
 }
 
 int gdn_scan_segments(int B, int T, int Hk, int Hv, int dk, int dv, int packed, unsigned flags) {
-  const unsigned known = GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u;
+  const unsigned known =
+      GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u | GDN_FLAG_SLICE32 | GDN_FLAG_SLICE64;
   if (check_sizes(B, T, Hk, Hv, dk, dv) != GDN_OK || (flags & ~known) != 0) return 0;
   if ((flags & GDN_FLAG_TWO_LEVEL) && (flags & GDN_FLAG_ONE_LEVEL)) return 0;
   int dev = 0, sms = 0;
@@ -495,11 +499,15 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
                    const int32_t* cu_seqlens, const float* init_state, void* out, float* final_state, int B,
                    int T, int Hk, int Hv, int dk, int dv, unsigned flags, void* stream) {
   t_last_cuda_error = 0;
-  const unsigned known = GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u;
+  const unsigned known =
+      GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u | GDN_FLAG_SLICE32 | GDN_FLAG_SLICE64;
   if ((flags & ~known) != 0) return GDN_ERR_ARG;
   if ((flags & GDN_FLAG_TWO_LEVEL) && (flags & GDN_FLAG_ONE_LEVEL)) return GDN_ERR_ARG;
+  if ((flags & GDN_FLAG_SLICE32) && (flags & GDN_FLAG_SLICE64)) return GDN_ERR_ARG;
   int rc = check_sizes(B, T, Hk, Hv, dk, dv);
   if (rc != GDN_OK) return rc;
+  if ((flags & GDN_FLAG_SLICE64) && dv % 64 != 0) return GDN_ERR_ARG;
+  const int slice = (flags & GDN_FLAG_SLICE32) ? 32 : (flags & GDN_FLAG_SLICE64) ? 64 : 0;
   if (B == 0) return GDN_OK;
   const long long ntok = cu_seqlens != nullptr ? (long long)T : (long long)B * T;
   if (ntok > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_ARG;
@@ -524,7 +532,8 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
     if (rc != GDN_OK) return rc;
   }
   return launch_all(q, k, v, g, beta, cu_seqlens, init_state, out, final_state, B, T, Hk, Hv, dk, dv,
-                    static_cast<cudaStream_t>(stream), ws, (flags & GDN_FLAG_L2NORM_QK) ? 1 : 0, &plan);
+                    static_cast<cudaStream_t>(stream), ws, (flags & GDN_FLAG_L2NORM_QK) ? 1 : 0, &plan, 0, -1, true,
+                    0, -1, 3, slice);
 }
 
 int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g, const float* beta,

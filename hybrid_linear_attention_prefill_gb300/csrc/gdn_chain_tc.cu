@@ -1,6 +1,6 @@
 // Chunk-sequential state carry on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// One CTA of 8 warps owns a 32-row slice of the dv x dk state S of one
+// One CTA of 8 warps owns a 32- or 64-row slice of the dv x dk state S of one
 // (sequence, value head) and walks the sequence's 64-token chunks in order.
 // For a chunk starting from S (rows beyond the chunk's n tokens are zero,
 // with g = beta = 0), with Tm = (I + A)^-1 and PT = P Tm from the preparation
@@ -58,71 +58,87 @@ namespace gdn {
 
 namespace {
 
-constexpr int kDVT = 32;        // state rows per CTA
 constexpr int kThreads = 288;   // 8 epilogue warps + 1 issue warp
 constexpr int kEpiThreads = 256;
-constexpr uint32_t kTmemCols = 128;
 constexpr int kParts = 2;       // accumulators in phase 1 (K = dk)
 constexpr int kParts23 = 1;     // and in phases 2 and 3 (K = 64)
 constexpr uint32_t kMaxPolls = 1u << 24;
 
-// stage layout (bytes)
-constexpr int kOffKQ = 0;                  // 2 x 16384
-constexpr int kOffTP = 32768;              // 16384
-constexpr int kOffV = kOffTP + 16384;      // 64 rows x 64 B (64 B swizzle)
-constexpr int kOffG = kOffV + 4096;        // 64 fp32
-constexpr int kOffB = kOffG + 256;         // 64 fp32
-constexpr int kOffRN = kOffB + 256;        // 128 fp32: inverse norms of the k rows, then the q rows
-constexpr int kStage = 54272;              // 53 KB, multiple of 1024
-constexpr int kStages = 3;                 // TMA ring: chunk c + 2 loads during chunk c
-static_assert(kOffRN + 512 <= kStage, "stage layout");
-// B operands after the stages
-constexpr int kOffS = kStages * kStage;    // 128 rows x 128 B
-constexpr int kOffR = kOffS + 16384;       // 64 rows x 128 B
-constexpr int kOffU = kOffR + 8192;        // 64 rows x 128 B
-constexpr int kOffBar = kOffU + 8192;      // 3 MMA mbarriers, 3 load mbarriers, TMEM base, abort flag
-constexpr int kSmemBytes = kOffBar + 64 + 1024;  // + slack for 1024-byte alignment
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// Layout of a CTA that owns DVT = 32 or 64 rows of the state.  The MMAs carry the bf16 hi and lo
+// parts of the slice along N = 2 DVT.  A 128-byte swizzle atom of an MN-major operand row holds
+// 64 bf16 = 32 state columns (16 hi, 16 lo per 16-column group), so the DVT = 64 operands are
+// two atoms wide, the second one atom's bytes after the first (the descriptor's leading byte
+// offset).
+template <int DVT>
+struct Cfg {
+  static constexpr int kN = 2 * DVT;
+  static constexpr int kAtoms = kN / 64;
+  static constexpr int kGroups = DVT / 32;            // 16-column groups per epilogue thread
+  static constexpr uint32_t kTmemCols = kParts * kN;   // phase 1's partial accumulators
+  // stage layout (bytes)
+  static constexpr int kOffKQ = 0;                  // 2 x 16384
+  static constexpr int kOffTP = 32768;              // 16384
+  static constexpr int kOffV = kOffTP + 16384;      // 64 rows x 2 DVT bytes (64 / 128 B swizzle)
+  static constexpr int kVBytes = 64 * 2 * DVT;
+  static constexpr int kOffG = kOffV + kVBytes;     // 64 fp32
+  static constexpr int kOffB = kOffG + 256;         // 64 fp32
+  static constexpr int kOffRN = kOffB + 256;        // 128 fp32: inverse norms of the k rows, then the q rows
+  static constexpr int kStage = (kOffRN + 512 + 1023) / 1024 * 1024;  // 53 KB (32 rows), 57 KB (64)
+  // TMA ring: chunk c + kStages - 1 loads during chunk c (two ahead with 32 rows; 64 rows leave
+  // room for two stages, so one ahead)
+  static constexpr int kStages = DVT == 32 ? 3 : 2;
+  // B operands after the stages: S (dk rows), R and dU (64 token rows), kAtoms atoms each
+  static constexpr int kAtomS = 128 * 128, kAtomRU = 64 * 128;
+  static constexpr int kOffS = kStages * kStage;
+  static constexpr int kOffR = kOffS + kAtoms * kAtomS;
+  static constexpr int kOffU = kOffR + kAtoms * kAtomRU;
+  // 64 rows: the Y rows of the output warps wait here between phases 1 and 2 ([32 columns][128 threads])
+  static constexpr int kOffY = kOffU + kAtoms * kAtomRU;
+  static constexpr int kYBytes = DVT == 64 ? 32 * 128 * 4 : 0;
+  static constexpr int kOffBar = kOffY + kYBytes;  // 3 MMA mbarriers, the load mbarriers, TMEM base, abort flag
+  static constexpr int kSmemBytes = kOffBar + 64 + 1024;   // + slack for 1024-byte alignment
+  static constexpr uint32_t kID_KS = tc::idesc_bf16(128, kN, 0, 1);  // A K-major, B MN-major
+  static constexpr uint32_t kID_KT = tc::idesc_bf16(128, kN, 1, 1);  // A MN-major, B MN-major
+  static_assert(DVT == 32 || DVT == 64, "32 or 64 state rows per CTA");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert((3 + kStages) * 8 <= 48, "mbarriers in the barrier block");
+};
 
-constexpr uint32_t kID_KS = tc::idesc_bf16(128, 2 * kDVT, 0, 1);  // A K-major, B MN-major
-constexpr uint32_t kID_KT = tc::idesc_bf16(128, 2 * kDVT, 1, 1);  // A MN-major, B MN-major
-
-// Write 16 fp32 values (state columns 16 cg .. 16 cg + 15) of one operand row as
-// bf16 hi parts (16-byte chunks 4 cg, 4 cg + 1) and lo parts (chunks 4 cg + 2, + 3),
-// so that accumulator columns 32 cg .. 32 cg + 31 hold this group's hi then lo sums.
-__device__ __forceinline__ void store_split16(unsigned char* tile, uint32_t row, int cg, const float (&x)[16]) {
+// Write 16 fp32 values (state columns 16 g .. 16 g + 15) of one operand row as bf16 hi parts and
+// lo parts: group g sits in swizzle atom g / 2 (atom_bytes apart), hi in 16-byte chunks
+// 4 (g % 2), + 1 and lo in + 2, + 3, so that accumulator columns 32 g .. 32 g + 31 hold this
+// group's hi then lo sums.
+__device__ __forceinline__ void store_split16(unsigned char* tile, int atom_bytes, uint32_t row, int g,
+                                              const float* x) {
+  tile += (g >> 1) * atom_bytes;
+  const int c = 4 * (g & 1);
   uint32_t h[8], l[8];
 #pragma unroll
   for (int p = 0; p < 8; ++p) split_bf16(x[2 * p], x[2 * p + 1], h[p], l[p]);
-  *reinterpret_cast<uint4*>(tile + tc::sw128(row, 4 * cg)) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(tile + tc::sw128(row, 4 * cg + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-  *reinterpret_cast<uint4*>(tile + tc::sw128(row, 4 * cg + 2)) = make_uint4(l[0], l[1], l[2], l[3]);
-  *reinterpret_cast<uint4*>(tile + tc::sw128(row, 4 * cg + 3)) = make_uint4(l[4], l[5], l[6], l[7]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, c)) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, c + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, c + 2)) = make_uint4(l[0], l[1], l[2], l[3]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, c + 3)) = make_uint4(l[4], l[5], l[6], l[7]);
 }
 
-// acc[i] = sum over the NP partial accumulators of the hi and lo products of
-// state column 16 cg + i (partial p holds columns 64 p + 32 cg ..: 16 hi, 16 lo).
-template <int NP>
-__device__ __forceinline__ void sum_parts(uint32_t taddr, int cg, float (&acc)[16]) {
-  if constexpr (NP == 2) {
+// acc[i] = sum over the NP partial accumulators (N columns apart) of the hi and lo products of
+// state column 16 g + i (partial p holds columns N p + 32 g ..: 16 hi, 16 lo).  With N = 64 two
+// partials are read by one TMEM load; with N = 128 one at a time, to hold fewer registers.
+template <int NP, int N>
+__device__ __forceinline__ void sum_parts(uint32_t taddr, int g, float (&acc)[16]) {
+  if constexpr (NP == 2 && N == 64) {
     float t[64];
-    tc::tmem_ld32x2(taddr + 32 * cg, taddr + 64 + 32 * cg, t);
+    tc::tmem_ld32x2(taddr + 32 * g, taddr + N + 32 * g, t);
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = (t[i] + t[16 + i]) + (t[32 + i] + t[48 + i]);
-  } else if constexpr (NP == 4) {
-    float t[128];
-    tc::tmem_ld32x4(taddr + 32 * cg, taddr + 64 + 32 * cg, taddr + 128 + 32 * cg, taddr + 192 + 32 * cg, t);
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      acc[i] = ((t[i] + t[16 + i]) + (t[32 + i] + t[48 + i])) + ((t[64 + i] + t[80 + i]) + (t[96 + i] + t[112 + i]));
   } else {
     float t[32];
-    tc::tmem_ld32(taddr + 32 * cg, t);
+    tc::tmem_ld32(taddr + 32 * g, t);
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = t[i] + t[16 + i];
 #pragma unroll
     for (int p = 1; p < NP; ++p) {
-      tc::tmem_ld32(taddr + 64 * p + 32 * cg, t);
+      tc::tmem_ld32(taddr + N * p + 32 * g, t);
 #pragma unroll
       for (int i = 0; i < 16; ++i) acc[i] += t[i] + t[16 + i];
     }
@@ -133,7 +149,10 @@ __device__ __forceinline__ void sum_parts(uint32_t taddr, int cg, float (&acc)[1
 
 // kNorm: q and k are normalised in-kernel (their inverse norms come from the
 // preparation kernel); a separate instantiation keeps the plain path free of it.
-template <int DK, bool kNorm>
+// One CTA per SM.  Nine warps leave three on one of the SM's four sub-partitions, whose 16 K
+// registers then cap a thread at 168: the 64-row slice reads its partial sums 32 columns at a
+// time to stay within it.
+template <int DK, bool kNorm, int DVT>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
@@ -143,23 +162,24 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     __nv_bfloat16* __restrict__ out,
                     float* fin, int* __restrict__ err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
                     long long nslots, int h_base, int c_begin, int c_end) {
+  using C = Cfg<DVT>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
   unsigned char* sm = smem_raw + pad;
   const uint32_t sb = raw_s + pad;  // shared-window address of sm
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);        // [0..2] MMA phases
-  uint64_t* full = bars + 3;                                          // [0..2] stage loaded
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 48);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffBar + 52);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);     // [0..2] MMA phases
+  uint64_t* full = bars + 3;                                          // [0..kStages) stage loaded
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffBar + 48);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffBar + 52);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 8;
   const int q4 = warp & 3;         // TMEM lane quadrant (epilogue warps)
-  const int cg = (warp >> 2) & 1;  // column group: state columns 16 cg .. 16 cg + 15
+  const int half = (warp >> 2) & 1;  // state columns 16 g .. 16 g + 15 for g = kGroups half + gg
   const int row = 32 * q4 + lane;
-  const int ntiles = DV / kDVT;
+  const int ntiles = DV / DVT;
   // CTA (x, y) = (sequence b x slices + slice, head).  With a dispatch order (packed batches),
   // the CTA's position in dispatch order walks the sequences most chunks first, and every
   // head and slice of one sequence before the next, so that the long chains start first.
@@ -173,13 +193,14 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     bx = (ob >= 0 && ob < B ? ob : r) * ntiles + rem % ntiles;
   }
   const int b = bx / ntiles;
-  const int dv0 = (bx - b * ntiles) * kDVT;
+  const int dv0 = (bx - b * ntiles) * DVT;
   const int h = h_base + hy;
   const int hk = h / (Hv / Hk);
   const float scale = rsqrtf((float)DK);
   constexpr int kP1 = DK / 16 < kParts ? DK / 16 : kParts;  // partials used by phase 1
   constexpr int kKBlocks = DK > 64 ? 2 : 1;                  // 64-wide d blocks loaded per tile
-  constexpr uint32_t kTxBytes = 2 * kKBlocks * 8192 + 4096 + 16384;
+  constexpr uint32_t kTxBytes = 2 * kKBlocks * 8192 + C::kVBytes + 16384;
+  constexpr int kAhead = C::kStages - 1;  // chunks whose tiles are in flight ahead of the current one
 
   const SeqChunk sq = seq_bounds(cu, b, T);
   const int slot0 = cu == nullptr ? b * nc_dense : chunk_off[b];
@@ -193,11 +214,11 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
   // ---- set-up: TMEM, barriers, zero d-block 1 when dk <= 64 --------------------
   if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_alloc(tmem_slot, C::kTmemCols);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 3 + kStages; ++i) tc::mbar_init(&bars[i], 1);
+    for (int i = 0; i < 3 + C::kStages; ++i) tc::mbar_init(&bars[i], 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -208,20 +229,25 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     tc::prefetch_tensormap(&tm_w);
   }
   if (kKBlocks == 1 && !issuer) {  // phase 3 reads all 128 rows of K^T: the rows d >= 64 stay zero
-    for (int e = tid; e < kStages * 1024; e += kEpiThreads) {
+    for (int e = tid; e < C::kStages * 1024; e += kEpiThreads) {
       const int stg = e >> 10, w = e & 1023;
-      *reinterpret_cast<uint4*>(sm + stg * kStage + kOffKQ + 16384 + w * 16) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sm + stg * C::kStage + C::kOffKQ + 16384 + w * 16) = make_uint4(0, 0, 0, 0);
     }
   }
 
-  // ---- initial state: thread (row d, cg) holds S[16 cg + i][d] -------------------
+  // ---- initial state: thread (row d, half) holds S[16 g + i][d], g = kGroups half + gg ----
   const int d = row;
-  float s[16];
+  float s[16 * C::kGroups];
   if (!issuer) {
-    const size_t base = ((size_t)b * Hv + h) * DV + dv0 + 16 * cg;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) s[i] = (init != nullptr && d < DK) ? init[(base + i) * DK + d] : 0.f;
-    store_split16(sm + kOffS, d, cg, s);
+    for (int gg = 0; gg < C::kGroups; ++gg) {
+      const int g = C::kGroups * half + gg;
+      const size_t base = ((size_t)b * Hv + h) * DV + dv0 + 16 * g;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        s[16 * gg + i] = (init != nullptr && d < DK) ? init[(base + i) * DK + d] : 0.f;
+      store_split16(sm + C::kOffS, C::kAtomS, d, g, s + 16 * gg);
+    }
   }
   tc::fence_proxy_async();
   tc::fence_before();
@@ -232,38 +258,36 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
   // TMA for the tiles of chunk c into stage stg (one thread); g and beta by cp.async.
   auto load_tiles = [&](int c, int stg) {
-    unsigned char* st = sm + stg * kStage;
+    unsigned char* st = sm + stg * C::kStage;
     const int t0 = (int)(sq.bos + (long long)c * kChunk);
     tc::mbar_arrive_expect_tx(&full[stg], kTxBytes);
 #pragma unroll
     for (int db = 0; db < kKBlocks; ++db) {
-      tc::tma_load_3d(st + kOffKQ + db * 16384, &tm_k, 64 * db, hk, t0, &full[stg]);
-      tc::tma_load_3d(st + kOffKQ + db * 16384 + 8192, &tm_q, 64 * db, hk, t0, &full[stg]);
+      tc::tma_load_3d(st + C::kOffKQ + db * 16384, &tm_k, 64 * db, hk, t0, &full[stg]);
+      tc::tma_load_3d(st + C::kOffKQ + db * 16384 + 8192, &tm_q, 64 * db, hk, t0, &full[stg]);
     }
-    tc::tma_load_3d(st + kOffV, &tm_v, dv0, h, t0, &full[stg]);
-    tc::tma_load_2d(st + kOffTP, &tm_w, 0, (int)(((long long)(slot0 + c) * Hv + h) * 128), &full[stg]);
+    tc::tma_load_3d(st + C::kOffV, &tm_v, dv0, h, t0, &full[stg]);
+    tc::tma_load_2d(st + C::kOffTP, &tm_w, 0, (int)(((long long)(slot0 + c) * Hv + h) * 128), &full[stg]);
   };
   auto load_scalars = [&](int c, int stg) {
-    unsigned char* st = sm + stg * kStage;
+    unsigned char* st = sm + stg * C::kStage;
     if (tid < kChunk) {
       const int n = min(kChunk, sq.len - c * kChunk);
       const bool ok = tid < n;
       const size_t off = ok ? (size_t)(sq.bos + (long long)c * kChunk + tid) * Hv + h : 0;
-      cp_async4(st + kOffG + 4 * tid, g + off, ok);
-      cp_async4(st + kOffB + 4 * tid, beta + off, ok);
+      cp_async4(st + C::kOffG + 4 * tid, g + off, ok);
+      cp_async4(st + C::kOffB + 4 * tid, beta + off, ok);
       if (kNorm) {  // the chunk's inverse norms, from the preparation kernel
         const float* rn = ws_rn + ((size_t)(slot0 + c) * Hk + hk) * (2 * kChunk);
-        cp_async4(st + kOffRN + 4 * tid, rn + tid, true);
-        cp_async4(st + kOffRN + 256 + 4 * tid, rn + kChunk + tid, true);
+        cp_async4(st + C::kOffRN + 4 * tid, rn + tid, true);
+        cp_async4(st + C::kOffRN + 256 + 4 * tid, rn + kChunk + tid, true);
       }
     }
   };
 
   if (c1 > c0) {
-    if (issuer && lane == 0) {
-      load_tiles(c0, 0);
-      if (c1 > c0 + 1) load_tiles(c0 + 1, 1);
-    }
+    if (issuer && lane == 0)
+      for (int a = 0; a < kAhead && c0 + a < c1; ++a) load_tiles(c0 + a, a);
     load_scalars(c0, 0);
   }
   cp_async_commit();
@@ -273,12 +297,12 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   int c = c0;
   for (; c < c1; ++c) {
     const int ci = c - c0;  // position in this launch: stage and barrier phases
-    const int stg = ci % kStages;
+    const int stg = ci % C::kStages;
     const uint32_t par = (uint32_t)(ci & 1);
-    unsigned char* st = sm + stg * kStage;
-    const uint32_t st_s = sb + stg * kStage;
+    unsigned char* st = sm + stg * C::kStage;
+    const uint32_t st_s = sb + stg * C::kStage;
     cp_async_wait<0>();
-    if (!tc::mbar_wait(&full[stg], (uint32_t)((ci / kStages) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
+    if (!tc::mbar_wait(&full[stg], (uint32_t)((ci / C::kStages) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
     __syncthreads();
     if (*abort_flag) { aborted = true; break; }
 
@@ -288,13 +312,14 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         tc::fence_after();
 #pragma unroll
         for (int ks = 0; ks < DK / 16; ++ks) {
-          const uint64_t a = tc::sdesc(st_s + kOffKQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSw128);
-          const uint64_t bd = tc::sdesc(sb + kOffS + ks * 2048, 0, 1024, tc::kSw128);
-          tc::mma_bf16(tmem + 64 * (ks % kP1), a, bd, kID_KS, ks >= kP1);
+          const uint64_t a = tc::sdesc(st_s + C::kOffKQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSw128);
+          const uint64_t bd = tc::sdesc(sb + C::kOffS + ks * 2048, C::kAtomS, 1024, tc::kSw128);
+          tc::mma_bf16(tmem + C::kN * (ks % kP1), a, bd, C::kID_KS, ks >= kP1);
         }
         tc::commit(&bars[0]);
-        // stage (ci + 2) % 3 was last read by the previous chunk's MMAs, which are done
-        if (c + 2 < c1) load_tiles(c + 2, (ci + 2) % kStages);
+        // stage (ci + kAhead) % kStages = (ci - 1) % kStages was last read by the previous
+        // chunk's MMAs, which are done
+        if (c + kAhead < c1) load_tiles(c + kAhead, (ci + kAhead) % C::kStages);
       }
       __syncwarp();
       __syncthreads();  // R written
@@ -304,9 +329,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         tc::fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = tc::sdesc(st_s + kOffTP + ks * 32, 16, 1024, tc::kSw128);
-          const uint64_t bd = tc::sdesc(sb + kOffR + ks * 2048, 0, 1024, tc::kSw128);
-          tc::mma_bf16(tmem + 64 * (ks % kParts23), a, bd, kID_KS, ks >= kParts23);
+          const uint64_t a = tc::sdesc(st_s + C::kOffTP + ks * 32, 16, 1024, tc::kSw128);
+          const uint64_t bd = tc::sdesc(sb + C::kOffR + ks * 2048, C::kAtomRU, 1024, tc::kSw128);
+          tc::mma_bf16(tmem + C::kN * (ks % kParts23), a, bd, C::kID_KS, ks >= kParts23);
         }
         tc::commit(&bars[1]);
       }
@@ -318,9 +343,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         tc::fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = tc::sdesc(st_s + kOffKQ + ks * 2048, 16384, 1024, tc::kSw128);
-          const uint64_t bd = tc::sdesc(sb + kOffU + ks * 2048, 0, 1024, tc::kSw128);
-          tc::mma_bf16(tmem + 64 * (ks % kParts23), a, bd, kID_KT, ks >= kParts23);
+          const uint64_t a = tc::sdesc(st_s + C::kOffKQ + ks * 2048, 16384, 1024, tc::kSw128);
+          const uint64_t bd = tc::sdesc(sb + C::kOffU + ks * 2048, C::kAtomRU, 1024, tc::kSw128);
+          tc::mma_bf16(tmem + C::kN * (ks % kParts23), a, bd, C::kID_KT, ks >= kParts23);
         }
         tc::commit(&bars[2]);
       }
@@ -329,12 +354,12 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     }
 
     // ================= epilogue warps =================
-    if (c + 1 < c1) load_scalars(c + 1, (ci + 1) % kStages);
+    if (c + 1 < c1) load_scalars(c + 1, (ci + 1) % C::kStages);
     cp_async_commit();
 
     // per-token scalars: every warp scans the 64 log decays of the chunk
-    const float* gs = reinterpret_cast<const float*>(st + kOffG);
-    const float* bs = reinterpret_cast<const float*>(st + kOffB);
+    const float* gs = reinterpret_cast<const float*>(st + C::kOffG);
+    const float* bs = reinterpret_cast<const float*>(st + C::kOffB);
     float g0 = gs[lane], g1 = gs[lane + 32];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -351,34 +376,47 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const float b_t = bs[tok];
     // with in-kernel q/k normalisation, this token's inverse norm (k rows for the
     // R / dU epilogues, q rows for the outputs), as the preparation kernel summed it
-    const float rn = kNorm ? reinterpret_cast<const float*>(st + kOffRN)[tok + (q4 < 2 ? 0 : 64)] : 1.f;
+    const float rn = kNorm ? reinterpret_cast<const float*>(st + C::kOffRN)[tok + (q4 < 2 ? 0 : 64)] : 1.f;
 
     // ---- phase-1 epilogue: R = beta V - beta e X (rows 0..63), keep Y (rows 64..127)
     if (!tc::mbar_wait(&bars[0], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
     tc::fence_after();
-    float acc[16], y[16];
-    sum_parts<kP1>(tq, cg, acc);
-    if (q4 < 2) {
-      const unsigned char* vrow = st + kOffV;
-      const float be = b_t * e_t * rn;
+    // Y rows of the output warps (q4 >= 2) until phase 2: 32 rows keep their one group in registers,
+    // 64 rows their two groups in shared memory (column-major over the 128 output threads)
+    float acc[16], y[1][16];
+    float* ys = reinterpret_cast<float*>(sm + C::kOffY) + (q4 >= 2 ? 32 * (q4 - 2) + lane + 64 * half : 0);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(vrow + tc::sw64(tok, 2 * cg + half));
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int gg = 0; gg < C::kGroups; ++gg) {
+      const int g = C::kGroups * half + gg;
+      sum_parts<kP1, C::kN>(tq, g, acc);
+      if (q4 < 2) {
+        const unsigned char* vrow = st + C::kOffV;
+        const float be = b_t * e_t * rn;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[p]));
-          const int i = 8 * half + 2 * p;
-          acc[i] = b_t * vv.x - be * acc[i];
-          acc[i + 1] = b_t * vv.y - be * acc[i + 1];
+        for (int hh = 0; hh < 2; ++hh) {  // the group's two 16-byte chunks of the value row
+          uint32_t voff;
+          if constexpr (DVT == 32) voff = tc::sw64(tok, 2 * g + hh);
+          else voff = tc::sw128(tok, 2 * g + hh);
+          const uint4 raw = *reinterpret_cast<const uint4*>(vrow + voff);
+          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[p]));
+            const int i = 8 * hh + 2 * p;
+            acc[i] = b_t * vv.x - be * acc[i];
+            acc[i + 1] = b_t * vv.y - be * acc[i + 1];
+          }
         }
-      }
-      store_split16(sm + kOffR, tok, cg, acc);
-      tc::fence_proxy_async();  // R is read by the tensor core next
-    } else {
+        store_split16(sm + C::kOffR, C::kAtomRU, tok, g, acc);
+      } else if constexpr (DVT == 32) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = acc[i] * rn;
+        for (int i = 0; i < 16; ++i) y[gg][i] = acc[i] * rn;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ys[(16 * gg + i) * 128] = acc[i] * rn;
+      }
     }
+    if (q4 < 2) tc::fence_proxy_async();  // R is read by the tensor core next
     tc::fence_before();
     __syncthreads();  // R written
     if (*abort_flag) { aborted = true; break; }
@@ -386,42 +424,65 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // ---- phase-2 epilogue: dU (rows 0..63); outputs from Z (rows 64..127) ------------
     if (!tc::mbar_wait(&bars[1], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
     tc::fence_after();
-    sum_parts<kParts23>(tq, cg, acc);
-    uint32_t o8[8];
-    if (q4 < 2) {
-      const float dr = d_t * rn;
+    uint32_t o8[C::kGroups][8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] *= dr;
-      store_split16(sm + kOffU, tok, cg, acc);
-      tc::fence_proxy_async();  // dU is read by the tensor core next
-    } else {
-      const float es = scale * e_t;
+    for (int gg = 0; gg < C::kGroups; ++gg) {
+      const int g = C::kGroups * half + gg;
+      sum_parts<kParts23, C::kN>(tq, g, acc);
+      if (q4 < 2) {
+        const float dr = d_t * rn;
 #pragma unroll
-      for (int p = 0; p < 8; ++p)
-        o8[p] = pack_bf16(es * y[2 * p] + scale * acc[2 * p], es * y[2 * p + 1] + scale * acc[2 * p + 1]);
+        for (int i = 0; i < 16; ++i) acc[i] *= dr;
+        store_split16(sm + C::kOffU, C::kAtomRU, tok, g, acc);
+      } else {
+        const float es = scale * e_t;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          float y0, y1;
+          if constexpr (DVT == 32) { y0 = y[gg][2 * p]; y1 = y[gg][2 * p + 1]; }
+          else { y0 = ys[(16 * gg + 2 * p) * 128]; y1 = ys[(16 * gg + 2 * p + 1) * 128]; }
+          o8[gg][p] = pack_bf16(es * y0 + scale * acc[2 * p], es * y1 + scale * acc[2 * p + 1]);
+        }
+        if constexpr (DVT == 64) {  // stored now: the packed outputs do not stay live across the barrier
+          const int n = min(kChunk, sq.len - c * kChunk);
+          if (tok < n) {
+            __nv_bfloat16* orow = out + ((size_t)(sq.bos + (long long)c * kChunk + tok) * Hv + h) * DV + dv0 + 16 * g;
+            *reinterpret_cast<uint4*>(orow) = make_uint4(o8[gg][0], o8[gg][1], o8[gg][2], o8[gg][3]);
+            *reinterpret_cast<uint4*>(orow + 8) = make_uint4(o8[gg][4], o8[gg][5], o8[gg][6], o8[gg][7]);
+          }
+        }
+      }
     }
+    if (q4 < 2) tc::fence_proxy_async();  // dU is read by the tensor core next
     tc::fence_before();
     __syncthreads();  // dU written
     if (*abort_flag) { aborted = true; break; }
 
     // outputs go out while the phase-3 MMAs run
-    if (q4 >= 2) {
+    if (DVT == 32 && q4 >= 2) {
       const int n = min(kChunk, sq.len - c * kChunk);
       if (tok < n) {
-        __nv_bfloat16* orow =
-            out + ((size_t)(sq.bos + (long long)c * kChunk + tok) * Hv + h) * DV + dv0 + 16 * cg;
-        *reinterpret_cast<uint4*>(orow) = make_uint4(o8[0], o8[1], o8[2], o8[3]);
-        *reinterpret_cast<uint4*>(orow + 8) = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+#pragma unroll
+        for (int gg = 0; gg < C::kGroups; ++gg) {
+          __nv_bfloat16* orow = out + ((size_t)(sq.bos + (long long)c * kChunk + tok) * Hv + h) * DV + dv0 +
+                                16 * (C::kGroups * half + gg);
+          *reinterpret_cast<uint4*>(orow) = make_uint4(o8[gg][0], o8[gg][1], o8[gg][2], o8[gg][3]);
+          *reinterpret_cast<uint4*>(orow + 8) = make_uint4(o8[gg][4], o8[gg][5], o8[gg][6], o8[gg][7]);
+        }
       }
     }
 
     // ---- phase-3 epilogue: S = e_last S + dS ------------------------------------------
     if (!tc::mbar_wait(&bars[2], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
     tc::fence_after();
-    sum_parts<kParts23>(tq, cg, acc);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) s[i] = fmaf(eC, s[i], acc[i]);
-    store_split16(sm + kOffS, d, cg, s);
+    for (int gg = 0; gg < C::kGroups; ++gg) {
+      const int g = C::kGroups * half + gg;
+      sum_parts<kParts23, C::kN>(tq, g, acc);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) s[16 * gg + i] = fmaf(eC, s[16 * gg + i], acc[i]);
+      store_split16(sm + C::kOffS, C::kAtomS, d, g, s + 16 * gg);
+    }
     tc::fence_proxy_async();  // S is read by the tensor core at the next chunk
     tc::fence_before();
   }
@@ -429,21 +490,24 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   // ---- final state, clean-up -------------------------------------------------------
   cp_async_wait<0>();
   if (!aborted && !issuer && fin != nullptr && d < DK) {
-    const size_t base = ((size_t)b * Hv + h) * DV + dv0 + 16 * cg;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) fin[(base + i) * DK + d] = s[i];
+    for (int gg = 0; gg < C::kGroups; ++gg) {
+      const size_t base = ((size_t)b * Hv + h) * DV + dv0 + 16 * (C::kGroups * half + gg);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) fin[(base + i) * DK + d] = s[16 * gg + i];
+    }
   }
   if (aborted && issuer && lane == 0) {
     // let MMAs and TMA copies still in flight land before the CTA exits (bounded again)
     const int ci = c - c0;
     const uint32_t par = (uint32_t)(ci & 1);
     for (int i = 0; i < 3; ++i) (void)tc::mbar_wait(&bars[i], par, 1u << 16);
-    for (int i = 0; i < kStages; ++i)
-      (void)tc::mbar_wait(&full[(ci + i) % kStages], (uint32_t)(((ci + i) / kStages) & 1), 1u << 16);
+    for (int i = 0; i < C::kStages; ++i)
+      (void)tc::mbar_wait(&full[(ci + i) % C::kStages], (uint32_t)(((ci + i) / C::kStages) & 1), 1u << 16);
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tc::tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // The bounded-wait path of the kernels, run on purpose: an mbarrier that nothing
@@ -491,16 +555,47 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 }  // namespace
 
+template <int DK, int DVT>
+cudaError_t launch_chain_tc_dvt(const CUtensorMap& mk, const CUtensorMap& mq, const void* v, const CUtensorMap& mw,
+                                const float* g, const float* beta, const int32_t* cu, const int32_t* chunk_off,
+                                const int32_t* order, const float* ws_rn, const float* init, void* out, float* fin,
+                                int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots,
+                                int norm_qk, int h_base, int h_count, int c_begin, int c_end, cuuint64_t tt,
+                                cudaStream_t st) {
+  using C = Cfg<DVT>;
+  CUtensorMap mv;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)DV, (cuuint64_t)Hv, tt};
+    const cuuint64_t strides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)Hv * DV * 2};
+    const cuuint32_t box[3] = {DVT, 1, 64};
+    if (!make_map(&mv, v, 3, dims, strides, box, DVT == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  auto* kernel = norm_qk ? gdn_chain_tc_kernel<DK, true, DVT> : gdn_chain_tc_kernel<DK, false, DVT>;
+  cudaError_t e = norm_qk ? set_smem_limit_once<gdn_chain_tc_kernel<DK, true, DVT>>(C::kSmemBytes)
+                          : set_smem_limit_once<gdn_chain_tc_kernel<DK, false, DVT>>(C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)B * (DV / DVT), h_count);  // value heads h_base .. h_base + h_count - 1
+  kernel<<<grid, kThreads, C::kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, order, ws_rn, init,
+                                                 static_cast<__nv_bfloat16*>(out), fin, err, B, T, Hk, Hv, DV,
+                                                 nc_dense, nslots, h_base, c_begin, c_end);
+  return cudaGetLastError();
+}
+
+// slice: state rows per CTA, 32 or 64, or 0 for the library's choice: 64 rows when dv allows it
+// and 32-row CTAs would take at least two waves of one CTA per SM (many sequences or heads:
+// each SM is then busy throughout, and a 64-row CTA issues the same MMAs at twice the width),
+// 32 otherwise (few CTAs: the chain latency decides, and more CTAs cover more SMs).
 template <int DK>
 cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const int32_t* cu, const int32_t* chunk_off, const int32_t* order, const void* ws,
                             const float* ws_rn, const float* init,
                             void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
                             long long nslots, int norm_qk, int h_base, int h_count, int c_begin, int c_end,
-                            cudaStream_t st) {
+                            int slice, cudaStream_t st) {
   const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
   const cuuint64_t tt = (cuuint64_t)(ttot > 0 ? ttot : 1);
-  CUtensorMap mk, mq, mv, mw;
+  CUtensorMap mk, mq, mw;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)Hk, tt};
     const cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)Hk * DK * 2};
@@ -510,27 +605,32 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
       return cudaErrorInvalidValue;
   }
   {
-    const cuuint64_t dims[3] = {(cuuint64_t)DV, (cuuint64_t)Hv, tt};
-    const cuuint64_t strides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)Hv * DV * 2};
-    const cuuint32_t box[3] = {kDVT, 1, 64};
-    if (!make_map(&mv, v, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B)) return cudaErrorInvalidValue;
-  }
-  {
     const long long rows = nslots * Hv * 128;
     const cuuint64_t dims[2] = {64, (cuuint64_t)(rows > 0 ? rows : 1)};
     const cuuint64_t strides[1] = {128};
     const cuuint32_t box[2] = {64, 128};
     if (!make_map(&mw, ws, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
   }
-  auto* kernel = norm_qk ? gdn_chain_tc_kernel<DK, true> : gdn_chain_tc_kernel<DK, false>;
-  cudaError_t e = norm_qk ? set_smem_limit_once<gdn_chain_tc_kernel<DK, true>>(kSmemBytes)
-                          : set_smem_limit_once<gdn_chain_tc_kernel<DK, false>>(kSmemBytes);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)B * (DV / kDVT), h_count);  // value heads h_base .. h_base + h_count - 1
-  kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, order, ws_rn, init,
-                                              static_cast<__nv_bfloat16*>(out), fin, err, B, T, Hk, Hv, DV,
-                                              nc_dense, nslots, h_base, c_begin, c_end);
-  return cudaGetLastError();
+  if (slice == 0) {
+    slice = 32;
+    if (DV % 64 == 0) {
+      int dev = 0, sms = 0;
+      cudaError_t e;
+      if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+      if ((long long)B * (DV / 32) * h_count >= 2LL * sms) slice = 64;
+    }
+  }
+  if (slice == 64) {
+    if (DV % 64 != 0) return cudaErrorInvalidValue;
+    return launch_chain_tc_dvt<DK, 64>(mk, mq, v, mw, g, beta, cu, chunk_off, order, ws_rn, init, out, fin, err, B,
+                                       T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end,
+                                       tt, st);
+  }
+  if (slice != 32) return cudaErrorInvalidValue;
+  return launch_chain_tc_dvt<DK, 32>(mk, mq, v, mw, g, beta, cu, chunk_off, order, ws_rn, init, out, fin, err, B, T,
+                                     Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, tt, st);
 }
 
 #define GDN_INST_CHAIN_TC(DK)                                                                                \
@@ -538,7 +638,7 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
                                            const int32_t*, const int32_t*, const int32_t*, const void*,       \
                                            const float*, const float*, void*,                                 \
                                            float*, int*, int, int, int, int, int, int, long long, int, int,   \
-                                           int, int, int, cudaStream_t);
+                                           int, int, int, int, cudaStream_t);
 GDN_INST_CHAIN_TC(32)
 GDN_INST_CHAIN_TC(64)
 GDN_INST_CHAIN_TC(128)

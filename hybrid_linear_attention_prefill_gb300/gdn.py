@@ -28,6 +28,8 @@ GDN_STATIC_SCRATCH_BYTES = 64 << 20
 GDN_FLAG_L2NORM_QK = 1
 GDN_FLAG_TWO_LEVEL = 2
 GDN_FLAG_ONE_LEVEL = 4
+GDN_FLAG_SLICE32 = 0x10000
+GDN_FLAG_SLICE64 = 0x20000
 GDN_STATUS_MMA_TIMEOUT = 1
 GDN_STATUS_LOAD_TIMEOUT = 2
 GDN_STATUS_PREP_LOAD_TIMEOUT = 4

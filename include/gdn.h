@@ -31,7 +31,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 3
+#define GDN_ABI_VERSION 4
 
 /* Status codes (0 = success, negative = error). */
 #define GDN_OK 0
@@ -47,6 +47,8 @@ extern "C" {
 #define GDN_FLAG_ONE_LEVEL 4u /* never use the two-level chunk scan */
 /* Segments per sequence for GDN_FLAG_TWO_LEVEL (2..255; 0 or absent = chosen by the library). */
 #define GDN_FLAG_SEGMENTS(n) ((((unsigned)(n)) & 0xffu) << 8)
+#define GDN_FLAG_SLICE32 0x10000u /* state carry: 32 state rows per CTA */
+#define GDN_FLAG_SLICE64 0x20000u /* state carry: 64 state rows per CTA (dv a multiple of 64) */
 
 /* Size of the fixed device scratch array behind gdn_prefill_static (64 MiB per device). */
 #define GDN_STATIC_SCRATCH_BYTES (64u << 20)
@@ -153,7 +155,14 @@ int gdn_prefill_host(const void *q, const void *k, const void *v,
  * whenever the batch is dense and has at least two chunks per sequence, with
  * GDN_FLAG_SEGMENTS(n) segments per sequence (capped at the chunk count) or, without
  * it, the library's choice (at least 3).  GDN_FLAG_ONE_LEVEL: never use it.  Both
- * together, or unknown flag bits, are GDN_ERR_ARG.  Everything else as gdn_prefill.
+ * together, or unknown flag bits, are GDN_ERR_ARG.
+ *
+ * GDN_FLAG_SLICE32 / GDN_FLAG_SLICE64: each state-carry CTA owns 32 or 64 rows of the
+ * dv x dk state.  Without either, the library takes 64 when dv is a multiple of 64 and
+ * 32-row CTAs would take at least two waves of one CTA per SM (many sequences or
+ * heads), else 32.  Both together, or GDN_FLAG_SLICE64 with dv = 32, are GDN_ERR_ARG.
+ * The results are the same either way up to rounding order.  Everything else as
+ * gdn_prefill.
  */
 int gdn_prefill_ex(const void *q, const void *k, const void *v,
                    const float *g, const float *beta,
