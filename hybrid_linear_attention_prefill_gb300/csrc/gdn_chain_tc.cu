@@ -582,10 +582,10 @@ cudaError_t launch_chain_tc_dvt(const CUtensorMap& mk, const CUtensorMap& mq, co
   return cudaGetLastError();
 }
 
-// slice: state rows per CTA, 32 or 64, or 0 for the library's choice: 64 rows when dv allows it
-// and 32-row CTAs would take at least two waves of one CTA per SM (many sequences or heads:
-// each SM is then busy throughout, and a 64-row CTA issues the same MMAs at twice the width),
-// 32 otherwise (few CTAs: the chain latency decides, and more CTAs cover more SMs).
+// slice: state rows per CTA, 32 or 64, or 0 for the library's choice.  A 64-row CTA issues the
+// same MMAs at twice the width, and its chunk step takes ~1.5x a 32-row one's: so 64 rows when dv
+// allows it and 1.5 x its waves of one CTA per SM are fewer than the 32-row grid's waves (many
+// sequences or heads), 32 otherwise (few CTAs: the chain latency decides).
 template <int DK>
 cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const int32_t* cu, const int32_t* chunk_off, const int32_t* order, const void* ws,
@@ -619,7 +619,9 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
       if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
           (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-      if ((long long)B * (DV / 32) * h_count >= 2LL * sms) slice = 64;
+      const long long n32 = (long long)B * (DV / 32) * h_count;
+      const long long waves32 = (n32 + sms - 1) / sms, waves64 = (n32 / 2 + sms - 1) / sms;
+      if (3 * waves64 < 2 * waves32) slice = 64;
     }
   }
   if (slice == 64) {

@@ -159,8 +159,8 @@ int gdn_prefill_host(const void *q, const void *k, const void *v,
  *
  * GDN_FLAG_SLICE32 / GDN_FLAG_SLICE64: each state-carry CTA owns 32 or 64 rows of the
  * dv x dk state.  Without either, the library takes 64 when dv is a multiple of 64 and
- * 32-row CTAs would take at least two waves of one CTA per SM (many sequences or
- * heads), else 32.  Both together, or GDN_FLAG_SLICE64 with dv = 32, are GDN_ERR_ARG.
+ * 1.5 x the waves (of one CTA per SM) of 64-row CTAs are fewer than those of 32-row
+ * CTAs (many sequences or heads), else 32.  Both together, or GDN_FLAG_SLICE64 with dv = 32, are GDN_ERR_ARG.
  * The results are the same either way up to rounding order.  Everything else as
  * gdn_prefill.
  */
