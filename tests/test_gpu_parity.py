@@ -238,6 +238,8 @@ def test_host_entry_matches_device_entry():
     dict(lengths=[1500, 0, 2600, 77], Hk=3, Hv=6, dk=128, dv=64, init_std=0.1),  # packed: 3 head groups
     dict(B=2, T=3000, Hk=8, Hv=8, dk=64, dv=128),                             # 2 sequences, ragged last chunk
     dict(B=1, T=4096, Hk=8, Hv=16, dk=32, dv=32, init_std=0.1),              # small head dims
+    # packed, 4 head groups whose state carries are large enough to run 64 state rows per CTA
+    dict(lengths=("uniform", 60, 50, 600), Hk=4, Hv=8, dk=128, dv=128, init_std=0.1),
 ])
 def test_host_entry_pipelined(case):
     """Large enough for gdn_prefill_host to overlap its copies with the kernels: token
