@@ -214,9 +214,11 @@ cudaError_t chain(const void* q, const void* k, const void* v, const float* g, c
                   const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* ws_rn,
                   const float* init, void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV,
                   int nc_dense, long long nslots, int norm_qk, cudaStream_t st) {
-  // the two-level scan's runs are packed views of segments: dispatched in their own order
+  // the two-level scan's runs are packed views of segments: dispatched in their own order, with
+  // 32 state rows per CTA (its choice of the segment count counts 32-row CTAs, so that pass A's
+  // two runs fit one wave side by side)
   return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, nullptr, tiles, ws_rn, init, out, fin, err, B, T,
-                                  Hk, Hv, DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, 0, st);
+                                  Hk, Hv, DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, 32, st);
 }
 
 cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -400,7 +402,8 @@ void gdn_set_phase_events(void* ev_begin, void* ev_mid, void* ev_end) {
 
 int gdn_scan_segments(int B, int T, int Hk, int Hv, int dk, int dv, int packed, unsigned flags) {
   const unsigned known =
-      GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u | GDN_FLAG_SLICE32 | GDN_FLAG_SLICE64;
+      GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u | GDN_FLAG_SLICE16 | GDN_FLAG_SLICE32 |
+      GDN_FLAG_SLICE64;
   if (check_sizes(B, T, Hk, Hv, dk, dv) != GDN_OK || (flags & ~known) != 0) return 0;
   if ((flags & GDN_FLAG_TWO_LEVEL) && (flags & GDN_FLAG_ONE_LEVEL)) return 0;
   int dev = 0, sms = 0;
@@ -500,14 +503,19 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
                    int T, int Hk, int Hv, int dk, int dv, unsigned flags, void* stream) {
   t_last_cuda_error = 0;
   const unsigned known =
-      GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u | GDN_FLAG_SLICE32 | GDN_FLAG_SLICE64;
+      GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u | GDN_FLAG_SLICE16 | GDN_FLAG_SLICE32 |
+      GDN_FLAG_SLICE64;
   if ((flags & ~known) != 0) return GDN_ERR_ARG;
   if ((flags & GDN_FLAG_TWO_LEVEL) && (flags & GDN_FLAG_ONE_LEVEL)) return GDN_ERR_ARG;
-  if ((flags & GDN_FLAG_SLICE32) && (flags & GDN_FLAG_SLICE64)) return GDN_ERR_ARG;
+  {
+    const unsigned sl = flags & (GDN_FLAG_SLICE16 | GDN_FLAG_SLICE32 | GDN_FLAG_SLICE64);
+    if (sl & (sl - 1)) return GDN_ERR_ARG;  // at most one slice width
+  }
   int rc = check_sizes(B, T, Hk, Hv, dk, dv);
   if (rc != GDN_OK) return rc;
   if ((flags & GDN_FLAG_SLICE64) && dv % 64 != 0) return GDN_ERR_ARG;
-  const int slice = (flags & GDN_FLAG_SLICE32) ? 32 : (flags & GDN_FLAG_SLICE64) ? 64 : 0;
+  const int slice =
+      (flags & GDN_FLAG_SLICE16) ? 16 : (flags & GDN_FLAG_SLICE32) ? 32 : (flags & GDN_FLAG_SLICE64) ? 64 : 0;
   if (B == 0) return GDN_OK;
   const long long ntok = cu_seqlens != nullptr ? (long long)T : (long long)B * T;
   if (ntok > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_ARG;

@@ -1,6 +1,6 @@
 // Chunk-sequential state carry on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// One CTA of 8 warps owns a 32- or 64-row slice of the dv x dk state S of one
+// One CTA of 8 warps owns a 16-, 32- or 64-row slice of the dv x dk state S of one
 // (sequence, value head) and walks the sequence's 64-token chunks in order.
 // For a chunk starting from S (rows beyond the chunk's n tokens are zero,
 // with g = beta = 0), with Tm = (I + A)^-1 and PT = P Tm from the preparation
@@ -64,29 +64,29 @@ constexpr int kParts = 2;       // accumulators in phase 1 (K = dk)
 constexpr int kParts23 = 1;     // and in phases 2 and 3 (K = 64)
 constexpr uint32_t kMaxPolls = 1u << 24;
 
-// Layout of a CTA that owns DVT = 32 or 64 rows of the state.  The MMAs carry the bf16 hi and lo
-// parts of the slice along N = 2 DVT.  A 128-byte swizzle atom of an MN-major operand row holds
-// 64 bf16 = 32 state columns (16 hi, 16 lo per 16-column group), so the DVT = 64 operands are
-// two atoms wide, the second one atom's bytes after the first (the descriptor's leading byte
-// offset).
+// Layout of a CTA that owns DVT = 16, 32 or 64 rows of the state.  The MMAs carry the bf16 hi
+// and lo parts of the slice along N = 2 DVT.  A 128-byte swizzle atom of an MN-major operand row
+// holds 64 bf16 = 32 state columns (16 hi, 16 lo per 16-column group), so the DVT = 64 operands
+// are two atoms wide, the second one atom's bytes after the first (the descriptor's leading byte
+// offset), and the DVT = 16 ones use the first 32 columns (before the swizzle) of each row.
 template <int DVT>
 struct Cfg {
   static constexpr int kN = 2 * DVT;
-  static constexpr int kAtoms = kN / 64;
-  static constexpr int kGroups = DVT / 32;            // 16-column groups per epilogue thread
+  static constexpr int kAtoms = (kN + 63) / 64;
+  static constexpr int kGroups = DVT / 32;            // 16-column groups per epilogue thread (16 rows: half of one)
   static constexpr uint32_t kTmemCols = kParts * kN;   // phase 1's partial accumulators
   // stage layout (bytes)
   static constexpr int kOffKQ = 0;                  // 2 x 16384
   static constexpr int kOffTP = 32768;              // 16384
-  static constexpr int kOffV = kOffTP + 16384;      // 64 rows x 2 DVT bytes (64 / 128 B swizzle)
+  static constexpr int kOffV = kOffTP + 16384;      // 64 rows x 2 DVT bytes (none / 64 / 128 B swizzle)
   static constexpr int kVBytes = 64 * 2 * DVT;
   static constexpr int kOffG = kOffV + kVBytes;     // 64 fp32
   static constexpr int kOffB = kOffG + 256;         // 64 fp32
   static constexpr int kOffRN = kOffB + 256;        // 128 fp32: inverse norms of the k rows, then the q rows
-  static constexpr int kStage = (kOffRN + 512 + 1023) / 1024 * 1024;  // 53 KB (32 rows), 57 KB (64)
-  // TMA ring: chunk c + kStages - 1 loads during chunk c (two ahead with 32 rows; 64 rows leave
-  // room for two stages, so one ahead)
-  static constexpr int kStages = DVT == 32 ? 3 : 2;
+  static constexpr int kStage = (kOffRN + 512 + 1023) / 1024 * 1024;  // 51, 53, 57 KB (16, 32, 64 rows)
+  // TMA ring: chunk c + kStages - 1 loads during chunk c (two ahead with 16 and 32 rows; 64 rows
+  // leave room for two stages, so one ahead)
+  static constexpr int kStages = DVT == 64 ? 2 : 3;
   // B operands after the stages: S (dk rows), R and dU (64 token rows), kAtoms atoms each
   static constexpr int kAtomS = 128 * 128, kAtomRU = 64 * 128;
   static constexpr int kOffS = kStages * kStage;
@@ -99,7 +99,7 @@ struct Cfg {
   static constexpr int kSmemBytes = kOffBar + 64 + 1024;   // + slack for 1024-byte alignment
   static constexpr uint32_t kID_KS = tc::idesc_bf16(128, kN, 0, 1);  // A K-major, B MN-major
   static constexpr uint32_t kID_KT = tc::idesc_bf16(128, kN, 1, 1);  // A MN-major, B MN-major
-  static_assert(DVT == 32 || DVT == 64, "32 or 64 state rows per CTA");
+  static_assert(DVT == 16 || DVT == 32 || DVT == 64, "16, 32 or 64 state rows per CTA");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert((3 + kStages) * 8 <= 48, "mbarriers in the barrier block");
 };
@@ -119,6 +119,32 @@ __device__ __forceinline__ void store_split16(unsigned char* tile, int atom_byte
   *reinterpret_cast<uint4*>(tile + tc::sw128(row, c + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
   *reinterpret_cast<uint4*>(tile + tc::sw128(row, c + 2)) = make_uint4(l[0], l[1], l[2], l[3]);
   *reinterpret_cast<uint4*>(tile + tc::sw128(row, c + 3)) = make_uint4(l[4], l[5], l[6], l[7]);
+}
+
+// 16-row CTAs: a thread owns 8 of the group's 16 columns, h = 0 or 1.  Its hi parts are 16-byte
+// chunk h of the operand row, its lo parts chunk 2 + h.
+__device__ __forceinline__ void store_split8(unsigned char* tile, uint32_t row, int h, const float* x) {
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) split_bf16(x[2 * p], x[2 * p + 1], hi[p], lo[p]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, h)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  *reinterpret_cast<uint4*>(tile + tc::sw128(row, 2 + h)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// acc[i] = sum over the NP partials (N columns apart) of the hi and lo products of state column
+// 8 h + i: hi in accumulator column 8 h + i, lo in 16 + 8 h + i.
+template <int NP, int N>
+__device__ __forceinline__ void sum_parts8(uint32_t taddr, int h, float (&acc)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    float hi[8], lo[8];
+    tc::tmem_ld8(taddr + N * p + 8 * h, hi);
+    tc::tmem_ld8(taddr + N * p + 16 + 8 * h, lo);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += hi[i] + lo[i];
+  }
 }
 
 // acc[i] = sum over the NP partial accumulators (N columns apart) of the hi and lo products of
@@ -236,8 +262,16 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   }
 
   // ---- initial state: thread (row d, half) holds S[16 g + i][d], g = kGroups half + gg ----
+  // (16 rows: S[8 half + i][d])
   const int d = row;
-  float s[16 * C::kGroups];
+  constexpr int kCols = DVT / 2;  // state columns per epilogue thread
+  float s[kCols];
+  if (!issuer && DVT == 16) {
+    const size_t base = ((size_t)b * Hv + h) * DV + dv0 + 8 * half;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] = (init != nullptr && d < DK) ? init[(base + i) * DK + d] : 0.f;
+    store_split8(sm + C::kOffS, d, half, s);
+  }
   if (!issuer) {
 #pragma unroll
     for (int gg = 0; gg < C::kGroups; ++gg) {
@@ -385,6 +419,25 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // 64 rows their two groups in shared memory (column-major over the 128 output threads)
     float acc[16], y[1][16];
     float* ys = reinterpret_cast<float*>(sm + C::kOffY) + (q4 >= 2 ? 32 * (q4 - 2) + lane + 64 * half : 0);
+    if constexpr (DVT == 16) {  // 8 columns a thread: value bytes 16 half of the 32-byte row
+      float a8[8];
+      sum_parts8<kP1, C::kN>(tq, half, a8);
+      if (q4 < 2) {
+        const float be = b_t * e_t * rn;
+        const uint4 raw = *reinterpret_cast<const uint4*>(st + C::kOffV + tok * 32 + 16 * half);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[p]));
+          a8[2 * p] = b_t * vv.x - be * a8[2 * p];
+          a8[2 * p + 1] = b_t * vv.y - be * a8[2 * p + 1];
+        }
+        store_split8(sm + C::kOffR, tok, half, a8);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[0][i] = a8[i] * rn;
+      }
+    }
 #pragma unroll
     for (int gg = 0; gg < C::kGroups; ++gg) {
       const int g = C::kGroups * half + gg;
@@ -424,7 +477,22 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // ---- phase-2 epilogue: dU (rows 0..63); outputs from Z (rows 64..127) ------------
     if (!tc::mbar_wait(&bars[1], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
     tc::fence_after();
-    uint32_t o8[C::kGroups][8];
+    uint32_t o8[C::kGroups > 0 ? C::kGroups : 1][8];
+    if constexpr (DVT == 16) {
+      float a8[8];
+      sum_parts8<kParts23, C::kN>(tq, half, a8);
+      if (q4 < 2) {
+        const float dr = d_t * rn;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a8[i] *= dr;
+        store_split8(sm + C::kOffU, tok, half, a8);
+      } else {
+        const float es = scale * e_t;
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          o8[0][p] = pack_bf16(es * y[0][2 * p] + scale * a8[2 * p], es * y[0][2 * p + 1] + scale * a8[2 * p + 1]);
+      }
+    }
 #pragma unroll
     for (int gg = 0; gg < C::kGroups; ++gg) {
       const int g = C::kGroups * half + gg;
@@ -459,6 +527,13 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     if (*abort_flag) { aborted = true; break; }
 
     // outputs go out while the phase-3 MMAs run
+    if (DVT == 16 && q4 >= 2) {
+      const int n = min(kChunk, sq.len - c * kChunk);
+      if (tok < n) {
+        __nv_bfloat16* orow = out + ((size_t)(sq.bos + (long long)c * kChunk + tok) * Hv + h) * DV + dv0 + 8 * half;
+        *reinterpret_cast<uint4*>(orow) = make_uint4(o8[0][0], o8[0][1], o8[0][2], o8[0][3]);
+      }
+    }
     if (DVT == 32 && q4 >= 2) {
       const int n = min(kChunk, sq.len - c * kChunk);
       if (tok < n) {
@@ -475,6 +550,13 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // ---- phase-3 epilogue: S = e_last S + dS ------------------------------------------
     if (!tc::mbar_wait(&bars[2], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
     tc::fence_after();
+    if constexpr (DVT == 16) {
+      float a8[8];
+      sum_parts8<kParts23, C::kN>(tq, half, a8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s[i] = fmaf(eC, s[i], a8[i]);
+      store_split8(sm + C::kOffS, d, half, s);
+    }
 #pragma unroll
     for (int gg = 0; gg < C::kGroups; ++gg) {
       const int g = C::kGroups * half + gg;
@@ -490,6 +572,11 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   // ---- final state, clean-up -------------------------------------------------------
   cp_async_wait<0>();
   if (!aborted && !issuer && fin != nullptr && d < DK) {
+    if constexpr (DVT == 16) {
+      const size_t base = ((size_t)b * Hv + h) * DV + dv0 + 8 * half;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) fin[(base + i) * DK + d] = s[i];
+    }
 #pragma unroll
     for (int gg = 0; gg < C::kGroups; ++gg) {
       const size_t base = ((size_t)b * Hv + h) * DV + dv0 + 16 * (C::kGroups * half + gg);
@@ -568,8 +655,9 @@ cudaError_t launch_chain_tc_dvt(const CUtensorMap& mk, const CUtensorMap& mq, co
     const cuuint64_t dims[3] = {(cuuint64_t)DV, (cuuint64_t)Hv, tt};
     const cuuint64_t strides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)Hv * DV * 2};
     const cuuint32_t box[3] = {DVT, 1, 64};
-    if (!make_map(&mv, v, 3, dims, strides, box, DVT == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
+    const CUtensorMapSwizzle swz =
+        DVT == 16 ? CU_TENSOR_MAP_SWIZZLE_NONE : DVT == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_map(&mv, v, 3, dims, strides, box, swz)) return cudaErrorInvalidValue;
   }
   auto* kernel = norm_qk ? gdn_chain_tc_kernel<DK, true, DVT> : gdn_chain_tc_kernel<DK, false, DVT>;
   cudaError_t e = norm_qk ? set_smem_limit_once<gdn_chain_tc_kernel<DK, true, DVT>>(C::kSmemBytes)
@@ -582,10 +670,12 @@ cudaError_t launch_chain_tc_dvt(const CUtensorMap& mk, const CUtensorMap& mq, co
   return cudaGetLastError();
 }
 
-// slice: state rows per CTA, 32 or 64, or 0 for the library's choice.  A 64-row CTA issues the
-// same MMAs at twice the width, and its chunk step takes ~1.5x a 32-row one's: so 64 rows when dv
-// allows it and 1.5 x its waves of one CTA per SM are fewer than the 32-row grid's waves (many
-// sequences or heads), 32 otherwise (few CTAs: the chain latency decides).
+// slice: state rows per CTA, 16, 32 or 64, or 0 for the library's choice.  A chunk step's MMA issue
+// and hand-offs do not depend on the width and its epilogues scale with it: a 64-row step takes
+// ~1.5x a 32-row one, a 16-row step ~0.75x.  So 64 rows when dv allows it and 1.5 x its waves of
+// one CTA per SM are fewer than the 32-row grid's waves (many sequences or heads); 16 rows when
+// twice the 32-row grid still fits one wave (few heads: the chain latency decides, and narrower
+// slices shorten it); 32 otherwise.
 template <int DK>
 cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const int32_t* cu, const int32_t* chunk_off, const int32_t* order, const void* ws,
@@ -613,7 +703,7 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
   }
   if (slice == 0) {
     slice = 32;
-    if (DV % 64 == 0) {
+    {
       int dev = 0, sms = 0;
       cudaError_t e;
       if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
@@ -621,7 +711,8 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
         return e;
       const long long n32 = (long long)B * (DV / 32) * h_count;
       const long long waves32 = (n32 + sms - 1) / sms, waves64 = (n32 / 2 + sms - 1) / sms;
-      if (3 * waves64 < 2 * waves32) slice = 64;
+      if (DV % 64 == 0 && 3 * waves64 < 2 * waves32) slice = 64;
+      else if (2 * n32 <= sms) slice = 16;
     }
   }
   if (slice == 64) {
@@ -630,6 +721,10 @@ cudaError_t launch_chain_tc(const void* q, const void* k, const void* v, const f
                                        T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end,
                                        tt, st);
   }
+  if (slice == 16)
+    return launch_chain_tc_dvt<DK, 16>(mk, mq, v, mw, g, beta, cu, chunk_off, order, ws_rn, init, out, fin, err, B,
+                                       T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end,
+                                       tt, st);
   if (slice != 32) return cudaErrorInvalidValue;
   return launch_chain_tc_dvt<DK, 32>(mk, mq, v, mw, g, beta, cu, chunk_off, order, ws_rn, init, out, fin, err, B, T,
                                      Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, tt, st);

@@ -29,6 +29,7 @@ GDN_FLAG_L2NORM_QK = 1
 GDN_FLAG_TWO_LEVEL = 2
 GDN_FLAG_ONE_LEVEL = 4
 GDN_FLAG_SLICE32 = 0x10000
+GDN_FLAG_SLICE16 = 0x40000
 GDN_FLAG_SLICE64 = 0x20000
 GDN_STATUS_MMA_TIMEOUT = 1
 GDN_STATUS_LOAD_TIMEOUT = 2

@@ -48,6 +48,7 @@ extern "C" {
 /* Segments per sequence for GDN_FLAG_TWO_LEVEL (2..255; 0 or absent = chosen by the library). */
 #define GDN_FLAG_SEGMENTS(n) ((((unsigned)(n)) & 0xffu) << 8)
 #define GDN_FLAG_SLICE32 0x10000u /* state carry: 32 state rows per CTA */
+#define GDN_FLAG_SLICE16 0x40000u /* state carry: 16 state rows per CTA */
 #define GDN_FLAG_SLICE64 0x20000u /* state carry: 64 state rows per CTA (dv a multiple of 64) */
 
 /* Size of the fixed device scratch array behind gdn_prefill_static (64 MiB per device). */
@@ -157,11 +158,13 @@ int gdn_prefill_host(const void *q, const void *k, const void *v,
  * it, the library's choice (at least 3).  GDN_FLAG_ONE_LEVEL: never use it.  Both
  * together, or unknown flag bits, are GDN_ERR_ARG.
  *
- * GDN_FLAG_SLICE32 / GDN_FLAG_SLICE64: each state-carry CTA owns 32 or 64 rows of the
- * dv x dk state.  Without either, the library takes 64 when dv is a multiple of 64 and
- * 1.5 x the waves (of one CTA per SM) of 64-row CTAs are fewer than those of 32-row
- * CTAs (many sequences or heads), else 32.  Both together, or GDN_FLAG_SLICE64 with dv = 32, are GDN_ERR_ARG.
- * The results are the same either way up to rounding order.  Everything else as
+ * GDN_FLAG_SLICE16 / GDN_FLAG_SLICE32 / GDN_FLAG_SLICE64: each state-carry CTA owns
+ * 16, 32 or 64 rows of the dv x dk state.  Without one, the library takes 64 when dv is
+ * a multiple of 64 and 1.5 x the waves (of one CTA per SM) of 64-row CTAs are fewer
+ * than those of 32-row CTAs (many sequences or heads), 16 when twice as many 32-row
+ * CTAs would still fit one wave (few heads), else 32.  More than one of them, or
+ * GDN_FLAG_SLICE64 with dv = 32, is GDN_ERR_ARG.
+ * The results are the same for every width.  Everything else as
  * gdn_prefill.
  */
 int gdn_prefill_ex(const void *q, const void *k, const void *v,

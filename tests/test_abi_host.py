@@ -117,13 +117,15 @@ def test_decode_argument_checks(lib):
 def test_prefill_ex_rejects_unknown_flags(lib):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, cu_seqlens=None, init_state=None,
              out=FAKE, final_state=None, B=1, T=64, Hk=1, Hv=1, dk=128, dv=128, stream=0)
-    for bad in (8, 1 << 18, 1 << 31, gdn.GDN_FLAG_TWO_LEVEL | gdn.GDN_FLAG_ONE_LEVEL,
-                gdn.GDN_FLAG_SLICE32 | gdn.GDN_FLAG_SLICE64):
+    for bad in (8, 1 << 19, 1 << 31, gdn.GDN_FLAG_TWO_LEVEL | gdn.GDN_FLAG_ONE_LEVEL,
+                gdn.GDN_FLAG_SLICE32 | gdn.GDN_FLAG_SLICE64, gdn.GDN_FLAG_SLICE16 | gdn.GDN_FLAG_SLICE32,
+                gdn.GDN_FLAG_SLICE16 | gdn.GDN_FLAG_SLICE64):
         assert gdn.gdn_prefill_ex(**a, flags=bad) == gdn.GDN_ERR_ARG
     # 64 state rows per CTA need dv to be a multiple of 64
     assert gdn.gdn_prefill_ex(**{**a, "dk": 32, "dv": 32}, flags=gdn.GDN_FLAG_SLICE64) == gdn.GDN_ERR_ARG
     for ok in (gdn.GDN_FLAG_L2NORM_QK, gdn.GDN_FLAG_TWO_LEVEL | gdn.GDN_FLAG_SEGMENTS(5), gdn.GDN_FLAG_ONE_LEVEL,
-               gdn.GDN_FLAG_SLICE32, gdn.GDN_FLAG_SLICE64, gdn.GDN_FLAG_SLICE64 | gdn.GDN_FLAG_L2NORM_QK):
+               gdn.GDN_FLAG_SLICE16, gdn.GDN_FLAG_SLICE32, gdn.GDN_FLAG_SLICE64,
+               gdn.GDN_FLAG_SLICE64 | gdn.GDN_FLAG_L2NORM_QK):
         assert gdn.gdn_prefill_ex(**{**a, "B": 0}, flags=ok) == gdn.GDN_OK
 
 
@@ -134,7 +136,8 @@ def test_segment_flag_encoding():
     assert gdn.GDN_FLAG_SEGMENTS(3) == 3 << 8 and gdn.GDN_FLAG_SEGMENTS(255) == 0xFF00
     assert (gdn.GDN_FLAG_TWO_LEVEL, gdn.GDN_FLAG_ONE_LEVEL) == (2, 4)
     assert "#define GDN_FLAG_SLICE32 0x10000u" in hdr and "#define GDN_FLAG_SLICE64 0x20000u" in hdr
-    assert (gdn.GDN_FLAG_SLICE32, gdn.GDN_FLAG_SLICE64) == (0x10000, 0x20000)
+    assert "#define GDN_FLAG_SLICE16 0x40000u" in hdr
+    assert (gdn.GDN_FLAG_SLICE16, gdn.GDN_FLAG_SLICE32, gdn.GDN_FLAG_SLICE64) == (0x40000, 0x10000, 0x20000)
 
 
 def test_allocation_failure_hook_counts_down(lib):

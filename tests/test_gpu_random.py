@@ -2,7 +2,7 @@
 
 Each case draws, from its own seed: dense or packed (with empty and single-token sequences among
 the lengths), the key/value head counts and their ratio, dk and dv, the decay scale, an initial
-state or none, and the entry flags (slice width 32 / 64 / the library's choice, in-kernel q/k
+state or none, and the entry flags (slice width 16 / 32 / 64 / the library's choice, in-kernel q/k
 normalisation).  Sizes stay small enough for the oracle to finish in about a second each, and
 large enough to span several chunks and a ragged tail."""
 
@@ -45,7 +45,8 @@ def _draw(seed, gdn):
         lengths[int(r.integers(0, n))] = 0
         lengths[int(r.integers(0, n))] = 1
         kw = dict(lengths=lengths)
-    flags = int(r.choice([0, gdn.GDN_FLAG_SLICE32] + ([gdn.GDN_FLAG_SLICE64] if dv % 64 == 0 else [])))
+    flags = int(r.choice([0, gdn.GDN_FLAG_SLICE16, gdn.GDN_FLAG_SLICE32] +
+                         ([gdn.GDN_FLAG_SLICE64] if dv % 64 == 0 else [])))
     if not normalize:
         flags |= gdn.GDN_FLAG_L2NORM_QK
     inp = make_gdn_inputs(Hk=Hk, Hv=Hv, dk=dk, dv=dv, seed=2000 + seed, g_scale=g_scale, init_std=init_std,

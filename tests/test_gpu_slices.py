@@ -1,8 +1,8 @@
-"""State-carry CTAs of 32 or 64 state rows (GDN_FLAG_SLICE32 / GDN_FLAG_SLICE64) against the
-oracle, and against each other bit for bit (GPU).  The library takes 64 rows on its own for grids of at
-least two waves (the packed 32-candidate workload's parity test runs that way); these force
-each width on small inputs: dense and packed batches, every dk with dv = 64 and 128, an initial
-state, many chunks, in-kernel q/k normalisation."""
+"""State-carry CTAs of 16, 32 or 64 state rows (GDN_FLAG_SLICE16 / 32 / 64) against the oracle,
+and against each other bit for bit (GPU).  The library takes 64 rows on its own for grids of many
+waves (the packed 32-candidate workload's parity test runs that way) and 16 for few heads (most
+small parity cases); these force each width on small inputs: dense and packed batches, every dk
+with dv = 32, 64 and 128, an initial state, many chunks, in-kernel q/k normalisation."""
 
 import numpy as np
 import pytest
@@ -41,18 +41,22 @@ def _both_widths_against_oracle(gdn, inp, extra=0, ref=None):
 
     o_ref, s_ref = ref if ref is not None else oracle.prefill_inputs(inp)
     res = {}
-    for name, flag in (("32", gdn.GDN_FLAG_SLICE32), ("64", gdn.GDN_FLAG_SLICE64)):
+    widths = [("16", gdn.GDN_FLAG_SLICE16), ("32", gdn.GDN_FLAG_SLICE32)]
+    if inp.dv % 64 == 0:
+        widths.append(("64", gdn.GDN_FLAG_SLICE64))
+    for name, flag in widths:
         o, s = _run(gdn, inp, flag | extra)
         eo, es = out_err(o, o_ref), state_err(s, s_ref)
         print(f"\n[slices] {inp.name or 'case'} rows {name}: out {eo:.3e} state {es:.3e}")
         assert np.all(np.isfinite(o)) and np.all(np.isfinite(s))
         assert eo <= OUT_TOL and es <= STATE_TOL, (name, eo, es)
         res[name] = (o, s)
-    # the two widths form every column's products in the same order: bit for bit the same
-    assert np.array_equal(res["32"][0], res["64"][0]) and np.array_equal(res["32"][1], res["64"][1])
+    # every width forms each column's products in the same order: bit for bit the same
+    for name in res:
+        assert np.array_equal(res["32"][0], res[name][0]) and np.array_equal(res["32"][1], res[name][1]), name
 
 
-@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (32, 64), (128, 64), (64, 128)])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (32, 64), (128, 64), (64, 128), (128, 32), (32, 32)])
 def test_dense_both_widths(gdn, dk, dv):
     inp = make_gdn_inputs(B=2, T=300, Hk=2, Hv=4, dk=dk, dv=dv, seed=dk + dv, init_std=0.1)
     _both_widths_against_oracle(gdn, inp)
