@@ -188,6 +188,10 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     __nv_bfloat16* __restrict__ out,
                     float* fin, int* __restrict__ err, int B, int T, int Hk, int Hv, int DV, int nc_dense,
                     long long nslots, int h_base, int c_begin, int c_end) {
+  // Launched as a programmatic dependent of the kernel before it in the stream (the preparation
+  // kernel): the CTA starts while that kernel's last CTAs run and waits here until it has
+  // completed and its writes are visible (otherwise this returns at once).
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   using C = Cfg<DVT>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -663,10 +667,21 @@ cudaError_t launch_chain_tc_dvt(const CUtensorMap& mk, const CUtensorMap& mq, co
   cudaError_t e = norm_qk ? set_smem_limit_once<gdn_chain_tc_kernel<DK, true, DVT>>(C::kSmemBytes)
                           : set_smem_limit_once<gdn_chain_tc_kernel<DK, false, DVT>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)B * (DV / DVT), h_count);  // value heads h_base .. h_base + h_count - 1
-  kernel<<<grid, kThreads, C::kSmemBytes, st>>>(mk, mq, mv, mw, g, beta, cu, chunk_off, order, ws_rn, init,
-                                                 static_cast<__nv_bfloat16*>(out), fin, err, B, T, Hk, Hv, DV,
-                                                 nc_dense, nslots, h_base, c_begin, c_end);
+  // value heads h_base .. h_base + h_count - 1; a programmatic dependent of the kernel before it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B * (DV / DVT), h_count);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, mk, mq, mv, mw, g, beta, cu, chunk_off, order, ws_rn, init,
+                         static_cast<__nv_bfloat16*>(out), fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, h_base,
+                         c_begin, c_end);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
