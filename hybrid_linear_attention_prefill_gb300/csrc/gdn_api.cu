@@ -18,7 +18,7 @@
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, int,
+                        void*, float*, void*, int, int*, int, int, int, int, int, int, int, int, int, int, int, int,
                         cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, int32_t*, int*, cudaStream_t);
 template <int DK>
@@ -26,6 +26,10 @@ cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*,
                             const int32_t*, const int32_t*, const void*, const float*, const float*, void*, float*,
                             int*, int, int, int, int, int, int, long long, int, int, int, int, int, int,
                             cudaStream_t);
+template <int DK>
+cudaError_t launch_chain_f16(const void*, const float*, const float*, const int32_t*, const int32_t*,
+                             const int32_t*, const void*, const void*, const float*, void*, float*, int*, int, int,
+                             int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int32_t*, int, int, int, int, int, int, int,
                              cudaStream_t);
@@ -87,10 +91,12 @@ long long num_slots(int B, int T, int packed) {
 
 // Workspace: [256 B status words][chunk table and dispatch order (chunk_table_bytes)]
 //            [Tm/PT tiles per (slot, value head)][inverse q/k norms per (slot, key head)]
-size_t ws_bytes_for(int B, int T, int Hk, int Hv, int packed) {
+//            [fp16 [K; Q] images per (slot, key head)]
+size_t ws_bytes_for(int B, int T, int Hk, int Hv, int dk, int packed) {
   const size_t table = gdn::chunk_table_bytes(B);
   const size_t ns = (size_t)num_slots(B, T, packed);
-  return 256 + table + ns * Hv * gdn::kWsPerSlotHead + ns * Hk * gdn::kWsNormPerSlotKHead;
+  return 256 + table + ns * Hv * gdn::kWsPerSlotHead + ns * Hk * gdn::kWsNormPerSlotKHead +
+         ns * Hk * gdn::kws_kq_bytes(dk);
 }
 
 using gdn::set_cuda_error;
@@ -209,27 +215,43 @@ int prepare_scan(int dev, int B, int T, int Hv, int dk, int dv, bool packed, uns
   return GDN_OK;
 }
 
+// The state carry of value heads [h_base, h_base + h_count): fp16 operands by default, bf16
+// hi / lo pairs when `wide` (then with q and k read from the inputs).
 template <int DK>
-cudaError_t chain(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                  const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* ws_rn,
-                  const float* init, void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV,
-                  int nc_dense, long long nslots, int norm_qk, cudaStream_t st) {
-  // the two-level scan's runs are packed views of segments: dispatched in their own order, with
-  // 32 state rows per CTA (its choice of the segment count counts 32-row CTAs, so that pass A's
-  // two runs fit one wave side by side)
-  return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, nullptr, tiles, ws_rn, init, out, fin, err, B, T,
-                                  Hk, Hv, DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, 32, st);
+cudaError_t carry(int wide, const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const int32_t* cu, const int32_t* chunk_off, const int32_t* order, const void* tiles,
+                  const float* ws_rn, const void* ws_kq, const float* init, void* out, float* fin, int* err, int B,
+                  int T, int Hk, int Hv, int DV, int nc_dense, long long nslots, int norm_qk, int h_base,
+                  int h_count, int c_begin, int c_end, int slice, cudaStream_t st) {
+  if (wide)
+    return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T,
+                                    Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, st);
+  return gdn::launch_chain_f16<DK>(v, g, beta, cu, chunk_off, order, tiles, ws_kq, init, out, fin, err, B, T, Hk,
+                                   Hv, DV, nc_dense, nslots, h_base, h_count, c_begin, c_end, slice, st);
 }
 
-cudaError_t chain_dk(int dk, const void* q, const void* k, const void* v, const float* g, const float* beta,
-                     const int32_t* cu, const int32_t* chunk_off, const void* tiles, const float* ws_rn,
-                     const float* init, void* out, float* fin, int* err, int B, int T, int Hk, int Hv, int DV,
-                     int nc_dense, long long nslots, int norm_qk, cudaStream_t st) {
+cudaError_t carry_dk(int dk, int wide, const void* q, const void* k, const void* v, const float* g,
+                     const float* beta, const int32_t* cu, const int32_t* chunk_off, const int32_t* order,
+                     const void* tiles, const float* ws_rn, const void* ws_kq, const float* init, void* out,
+                     float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots,
+                     int norm_qk, int h_base, int h_count, int c_begin, int c_end, int slice, cudaStream_t st) {
   switch (dk) {
-    case 32: return chain<32>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
-    case 64: return chain<64>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
-    default: return chain<128>(q, k, v, g, beta, cu, chunk_off, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, st);
+    case 32: return carry<32>(wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, st);
+    case 64: return carry<64>(wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, st);
+    default: return carry<128>(wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, st);
   }
+}
+
+// A run of the two-level scan.  Its runs are packed views of segments: dispatched in their own
+// order, with 32 state rows per CTA (its choice of the segment count counts 32-row CTAs, so that
+// pass A's two runs fit one wave side by side).
+cudaError_t chain_dk(int dk, int wide, const void* q, const void* k, const void* v, const float* g,
+                     const float* beta, const int32_t* cu, const int32_t* chunk_off, const void* tiles,
+                     const float* ws_rn, const void* ws_kq, const float* init, void* out, float* fin, int* err,
+                     int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots, int norm_qk,
+                     cudaStream_t st) {
+  return carry_dk(dk, wide, q, k, v, g, beta, cu, chunk_off, nullptr, tiles, ws_rn, ws_kq, init, out, fin, err, B, T,
+                  Hk, Hv, DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, 32, st);
 }
 
 // The prefill for value heads [h0, h1) (all heads when h1 < 0; h0 and h1 multiples of
@@ -238,11 +260,12 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
                const int32_t* cu, const float* init, void* out, float* fin, int B, int T, int Hk, int Hv,
                int dk, int dv, cudaStream_t st, void* ws, int norm_qk = 0, const ScanPlan* plan = nullptr,
                int h0 = 0, int h1 = -1, bool table = true, int c0 = 0, int c1 = -1, int phases = 3,
-               int slice = 0) {
+               int slice = 0, int wide = 0) {
   // [h0, h1): value heads; [c0, c1): the window of each dense sequence's chunks (-1: all).
   // A window's launches carry the state from `init` to `fin` over its chunks only.
   // phases: bit 0 the preparation kernel (and the packed chunk table), bit 1 the state carry.
-  // slice: state rows per state-carry CTA (32, 64; 0 = the library's choice).
+  // slice: state rows per state-carry CTA (16, 32, 64; 0 = the library's choice).
+  // wide: the bf16 hi / lo state carry (fp32 range) instead of the fp16 one.
   if (h1 < 0) h1 = Hv;
   const int G = Hv / Hk;
   const int hk0 = h0 / G, nhk = (h1 - h0) / G;
@@ -261,6 +284,7 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   // entry's pipeline runs beside other pieces' kernels
   const int alone = whole && h0 == 0 && h1 == Hv && phases == 3;
   float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
+  void* ws_kq = reinterpret_cast<unsigned char*>(ws_rn) + (size_t)nslots * Hk * gdn::kWsNormPerSlotKHead;
   cudaError_t e = cudaSuccess;
   if (packed && table && (phases & 1)) {
     e = gdn::launch_chunk_table(cu, B, T, chunk_off, order, err, st);
@@ -272,9 +296,9 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
   if (nslots > 0x7fffffffLL) return GDN_ERR_ARG;
   if (nslots > 0 && (phases & 1)) {
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, alone, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, alone, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, alone, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, ws_kq, !wide, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, alone, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, ws_kq, !wide, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, alone, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu, chunk_off, tiles, ws_rn, ws_kq, !wide, err, B, T, Hk, Hv, (int)nslots, nc_dense, norm_qk, hk0, nhk, c0, c1 - c0, alone, st); break;
     }
     if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   }
@@ -312,19 +336,19 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     // true initial state: its outputs are final) beside the transition runs of 1 .. BP-2
     // (v = 0 from the identity, dk rows) on the second stream
     if (BP - 2 >= 1 &&
-        (e = chain_dk(dk, q, k, vzero, g, beta, cu_seg + 1, off_seg + 1, tiles, ws_rn, i_init + pi, oscr, phi + pi, err,
-                      BP - 2, ttot, Hk, Hv, dk, nc_dense, nslots, norm_qk, plan->aux)) != cudaSuccess)
+        (e = chain_dk(dk, wide, q, k, vzero, g, beta, cu_seg + 1, off_seg + 1, tiles, ws_rn, ws_kq, i_init + pi, oscr,
+                      phi + pi, err, BP - 2, ttot, Hk, Hv, dk, nc_dense, nslots, norm_qk, plan->aux)) != cudaSuccess)
       return set_cuda_error(e, GDN_ERR_LAUNCH);
-    if ((e = chain_dk(dk, q, k, v, g, beta, cu_seg, off_seg, tiles, ws_rn, a_init, out, n_fin, err, BP - 1, ttot, Hk, Hv,
-                      dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess ||
+    if ((e = chain_dk(dk, wide, q, k, v, g, beta, cu_seg, off_seg, tiles, ws_rn, ws_kq, a_init, out, n_fin, err, BP - 1,
+                      ttot, Hk, Hv, dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess ||
         (e = cudaEventRecord(plan->join, plan->aux)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(st, plan->join, 0)) != cudaSuccess)
       return set_cuda_error(e, GDN_ERR_LAUNCH);
     // segment start states, then pass C over segments 1 .. BP-1 (the outputs; the last
     // segment's final state)
     if ((e = gdn::launch_seg_combine(init, n_fin, phi, c_init, B, P, Hv, dv, dk, st)) != cudaSuccess ||
-        (e = chain_dk(dk, q, k, v, g, beta, cu_seg + 1, off_seg + 1, tiles, ws_rn, c_init + ps, out, f_fin + ps, err,
-                      BP - 1, ttot, Hk, Hv, dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess)
+        (e = chain_dk(dk, wide, q, k, v, g, beta, cu_seg + 1, off_seg + 1, tiles, ws_rn, ws_kq, c_init + ps, out,
+                      f_fin + ps, err, BP - 1, ttot, Hk, Hv, dv, nc_dense, nslots, norm_qk, st)) != cudaSuccess)
       return set_cuda_error(e, GDN_ERR_LAUNCH);
     if (fin != nullptr) {
       const size_t per = (size_t)Hv * dv * dk;
@@ -337,11 +361,8 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
     return GDN_OK;
   }
-  switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, slice, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, slice, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T, Hk, Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, slice, st); break;
-  }
+  e = carry_dk(dk, wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk,
+               Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, slice, st);
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   return GDN_OK;
@@ -403,7 +424,7 @@ void gdn_set_phase_events(void* ev_begin, void* ev_mid, void* ev_end) {
 int gdn_scan_segments(int B, int T, int Hk, int Hv, int dk, int dv, int packed, unsigned flags) {
   const unsigned known =
       GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u | GDN_FLAG_SLICE16 | GDN_FLAG_SLICE32 |
-      GDN_FLAG_SLICE64;
+      GDN_FLAG_SLICE64 | GDN_FLAG_WIDE_RANGE;
   if (check_sizes(B, T, Hk, Hv, dk, dv) != GDN_OK || (flags & ~known) != 0) return 0;
   if ((flags & GDN_FLAG_TWO_LEVEL) && (flags & GDN_FLAG_ONE_LEVEL)) return 0;
   int dev = 0, sms = 0;
@@ -417,7 +438,7 @@ int gdn_scan_segments(int B, int T, int Hk, int Hv, int dk, int dv, int packed, 
 
 size_t gdn_workspace_bytes(int B, int T, int Hk, int Hv, int dk, int dv, int packed) {
   if (check_sizes(B, T, Hk, Hv, dk, dv) != GDN_OK) return 0;
-  return ws_bytes_for(B, T, Hk, Hv, packed);
+  return ws_bytes_for(B, T, Hk, Hv, dk, packed);
 }
 
 int gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -444,7 +465,7 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevBuffers& d = g_dev[dev];
-    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hk, Hv, cu_seqlens != nullptr));
+    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hk, Hv, dk, cu_seqlens != nullptr));
     if (rc != GDN_OK) return rc;
     ws = d.ws;
     rc = prepare_scan(dev, B, T, Hv, dk, dv, cu_seqlens != nullptr, 0u, static_cast<cudaStream_t>(stream), plan);
@@ -471,7 +492,7 @@ int gdn_prefill_ws(const void* q, const void* k, const void* v, const float* g, 
   if (ntok == 0 && final_state == nullptr) return GDN_OK;
   if (workspace == nullptr) return GDN_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGN;
-  if (workspace_bytes < ws_bytes_for(B, T, Hk, Hv, cu_seqlens != nullptr)) return GDN_ERR_SCRATCH;
+  if (workspace_bytes < ws_bytes_for(B, T, Hk, Hv, dk, cu_seqlens != nullptr)) return GDN_ERR_SCRATCH;
   return launch_all(q, k, v, g, beta, cu_seqlens, init_state, out, final_state, B, T, Hk, Hv, dk, dv,
                     static_cast<cudaStream_t>(stream), workspace);
 }
@@ -504,7 +525,7 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
   t_last_cuda_error = 0;
   const unsigned known =
       GDN_FLAG_L2NORM_QK | GDN_FLAG_TWO_LEVEL | GDN_FLAG_ONE_LEVEL | 0xff00u | GDN_FLAG_SLICE16 | GDN_FLAG_SLICE32 |
-      GDN_FLAG_SLICE64;
+      GDN_FLAG_SLICE64 | GDN_FLAG_WIDE_RANGE;
   if ((flags & ~known) != 0) return GDN_ERR_ARG;
   if ((flags & GDN_FLAG_TWO_LEVEL) && (flags & GDN_FLAG_ONE_LEVEL)) return GDN_ERR_ARG;
   {
@@ -533,7 +554,7 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevBuffers& d = g_dev[dev];
-    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hk, Hv, cu_seqlens != nullptr));
+    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hk, Hv, dk, cu_seqlens != nullptr));
     if (rc != GDN_OK) return rc;
     ws = d.ws;
     rc = prepare_scan(dev, B, T, Hv, dk, dv, cu_seqlens != nullptr, flags, static_cast<cudaStream_t>(stream), plan);
@@ -541,7 +562,7 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
   }
   return launch_all(q, k, v, g, beta, cu_seqlens, init_state, out, final_state, B, T, Hk, Hv, dk, dv,
                     static_cast<cudaStream_t>(stream), ws, (flags & GDN_FLAG_L2NORM_QK) ? 1 : 0, &plan, 0, -1, true,
-                    0, -1, 3, slice);
+                    0, -1, 3, slice, (flags & GDN_FLAG_WIDE_RANGE) ? 1 : 0);
 }
 
 int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -589,7 +610,7 @@ int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g
     dp = &d;
     rc = ensure(d.stage, d.stage_bytes, total);
     if (rc != GDN_OK) return rc;
-    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hk, Hv, cu_seqlens != nullptr));
+    rc = ensure(d.ws, d.ws_bytes, ws_bytes_for(B, T, Hk, Hv, dk, cu_seqlens != nullptr));
     if (rc != GDN_OK) return rc;
     base = static_cast<unsigned char*>(d.stage);
     ws = d.ws;

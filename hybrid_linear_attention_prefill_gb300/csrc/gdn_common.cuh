@@ -12,15 +12,21 @@ namespace gdn {
 constexpr int kChunk = 64;  // tokens per chunk
 
 // ---------------------------------------------------------------------------
-// Workspace layout, per (chunk slot, value head): the bf16 UT-transform matrix
-// Tm = (I + A)^-1 and the decayed score product PT = P Tm, both 64 x 64 row-major.
+// Workspace layout, per (chunk slot, value head): the UT-transform matrix Tm = (I + A)^-1
+// and the decayed score product PT = P Tm, both 64 x 64 row-major, fp16 for the default
+// state carry and bf16 for the wide-range one.
 // ---------------------------------------------------------------------------
-constexpr int kWsTileElems = kChunk * kChunk;           // 4096 bf16
+constexpr int kWsTileElems = kChunk * kChunk;           // 4096 16-bit elements
 constexpr size_t kWsPerSlotHead = 2 * kWsTileElems * 2;  // bytes (Tm + PT)
 // After the tiles, per (chunk slot, key head): the inverse L2 norms of the chunk's
 // k rows then q rows (fp32, 64 + 64), written by the preparation kernel when q and k
 // are normalised in-kernel.
 constexpr size_t kWsNormPerSlotKHead = 2 * kChunk * 4;  // bytes
+// After the norms, per (chunk slot, key head), for the fp16 state carry: the chunk's k rows
+// then q rows as fp16 (normalised when q and k are normalised in-kernel), stored as the image
+// of the shared-memory tile the state carry reads -- [dk/64 blocks of 16 KiB][128 rows][128 B],
+// 128-byte swizzle, rows past the chunk's tokens zero -- so that one bulk copy restores it.
+__host__ __device__ constexpr size_t kws_kq_bytes(int dk) { return (dk > 64 ? 2 : 1) * (size_t)16384; }
 // Before the tiles (after 256 bytes of status words): the packed chunk table, B + 1 int32
 // chunk offsets, then the B sequences in the order their state carries are dispatched
 // (most chunks first), padded to 256 bytes.

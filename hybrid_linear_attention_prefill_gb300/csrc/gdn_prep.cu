@@ -10,8 +10,11 @@
 //   P  = lower_incl( (Q K^T) * Gamma )                   (decayed intra-chunk scores)
 //   PT = P Tm
 //
-// Tm and PT are stored as bf16 64 x 64 tiles in the workspace; the state-carry
-// kernel combines them with the state.  The pages only name the operation (the
+// Tm and PT are stored as 64 x 64 tiles in the workspace -- fp16 for the default
+// state carry, bf16 for the wide-range one -- and the state-carry kernel combines
+// them with the state.  For the fp16 state carry the kernel also writes the chunk's
+// k and q rows as fp16 (normalised when asked to), since a tensor-core product takes
+// both operands in one format.  The pages only name the operation (the
 // "chunked Gated DeltaNet prefill" of the "Open-Jev-27B-v1.1 native text
 // worker" page, "Validation and optimization scope"); the WY form is the
 // standard chunked rewriting of S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T.
@@ -25,10 +28,8 @@
 // taken (gamma_t - gamma_i, i <= t), so nothing overflows however strong the decay.
 #include <atomic>
 #include <cuda_fp16.h>
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "gdn_tc.cuh"
+#include "gdn_tmap.cuh"
 
 namespace gdn {
 
@@ -71,6 +72,27 @@ __device__ __forceinline__ void mma_f16x1(float (&acc)[4], const float* X, int l
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Two values as the 16-bit format of the stored tiles: fp16 or bf16.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float a, float b) {
+  if constexpr (F16) return pack_f16(a, b);
+  else return pack_bf16(a, b);
+}
+
+// d += a b for one m16n8k16 fragment triple (ldmatrix layouts) of fp16 or bf16 values.
+template <bool F16>
+__device__ __forceinline__ void mma16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    mma_bf16(d, a, b0, b1);
+  }
+}
+
 // Store a 16 x 8 accumulator tile (times `sgn`) at D[r0.., n0..].
 __device__ __forceinline__ void store_tile(float* D, int ldd, int r0, int n0, const float (&acc)[4], float sgn,
                                            int lane) {
@@ -83,11 +105,11 @@ __device__ __forceinline__ void store_tile(float* D, int ldd, int r0, int n0, co
 
 template <int DK>
 struct PrepSmem {
-  // [union: K,Q tiles (TMA, 128 B swizzle) | A,Tm fp32] [P bf16] [Tm bf16 | decay tables |
+  // [union: K,Q tiles (TMA, 128 B swizzle) | A,Tm fp32] [P 16-bit] [Tm 16-bit | decay tables |
   // merge buffer] [inverse norms] [column factors] [g, beta] [mbarriers]
   // (the Grams stay in TMEM; the CTA fits four times on an SM).  Within a value head the decay
   // tables live until A and P are built, the merge buffer through the 16 -> 32 -> 64 merges and
-  // the bf16 Tm from then on, so the three share one region.
+  // the 16-bit Tm from then on, so the three share one region.
   static constexpr int kKQBytes = 32768;
   static constexpr int kATBytes = 2 * kChunk * LDF * 4;
   static constexpr int kUnion = kKQBytes > kATBytes ? kKQBytes : kATBytes;
@@ -95,20 +117,22 @@ struct PrepSmem {
   static constexpr int offTb = offP + kChunk * LDB * 2;
   static constexpr int offW = offTb;                   // the merge buffer, over the bf16 Tm
   static constexpr int offRN = offTb + kChunk * LDB * 2;  // inverse norms of k rows, then q rows
-  static_assert(32 * LDW * 4 <= kChunk * LDB * 2, "the merge buffer fits over the bf16 Tm");
-  static_assert(4 * 16 * LDE * 4 + kChunk * 4 * 4 <= kChunk * LDB * 2, "the decay tables fit over the bf16 Tm");
+  static_assert(32 * LDW * 4 <= kChunk * LDB * 2, "the merge buffer fits over the 16-bit Tm");
+  static_assert(4 * 16 * LDE * 4 + kChunk * 4 * 4 <= kChunk * LDB * 2, "the decay tables fit over the 16-bit Tm");
   static constexpr int offCF = offRN + 2 * kChunk * 4;  // column factors [64]
   static constexpr int offGB = offCF + kChunk * 4;       // [2 buffers][g 64 | beta 64] fp32
   static constexpr int offBar = offGB + 2 * 2 * kChunk * 4;
   static constexpr int bytes = offBar + 32 + 1024;  // 2 mbarriers + TMEM base; + slack for 1024-byte alignment
 };
 
-template <int DK>
+// F16: Tm, P and PT in fp16, and the fp16 [K; Q] image for the state carry (ws_kq); else bf16.
+template <int DK, bool F16>
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                 const float* __restrict__ g, const float* __restrict__ beta,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_off,
-                __nv_bfloat16* __restrict__ ws, float* __restrict__ ws_rn, int* __restrict__ err, int B,
+                uint16_t* __restrict__ ws, float* __restrict__ ws_rn, unsigned char* __restrict__ ws_kq,
+                int* __restrict__ err, int B,
                 int T, int Hk, int Hv, int nc_dense, int norm_qk, int hk_base, int hk_count, int c_begin,
                 int c_count, int n_items) {
   using L = PrepSmem<DK>;
@@ -118,8 +142,8 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   unsigned char* KQ = smem;                    // [2][128][128 B], swizzled
   float* As = reinterpret_cast<float*>(smem);  // aliases K/Q after the Grams
   float* Tms = As + kChunk * LDF;
-  __nv_bfloat16* Ps = reinterpret_cast<__nv_bfloat16*>(smem + L::offP);
-  __nv_bfloat16* Tmb = reinterpret_cast<__nv_bfloat16*>(smem + L::offTb);
+  uint16_t* Ps = reinterpret_cast<uint16_t*>(smem + L::offP);
+  uint16_t* Tmb = reinterpret_cast<uint16_t*>(smem + L::offTb);
   float* Wt = reinterpret_cast<float*>(smem + L::offW);  // [32][LDW]
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::offBar);  // [0] tiles loaded, [1] Grams done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offBar + 16);
@@ -127,7 +151,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   float* rnk = reinterpret_cast<float*>(smem + L::offRN);  // 1/||k_t|| (1 without normalisation)
   float* rnq = rnk + kChunk;                                // 1/||q_t||
   float* cfs = reinterpret_cast<float*>(smem + L::offCF);  // 1/||k_i|| 2^(gamma2_{i | 15} - gamma2_i)
-  // Decay tables of a value head, over the bf16 Tm (not in use while A and P are built):
+  // Decay tables of a value head, over the 16-bit Tm (not in use while A and P are built):
   // Es[b][r][c] = 2^(gamma2_{16b+r} - gamma2_{16b+c}) / ||k_{16b+c}|| for c <= r (else 0), and
   // rfs[t][b] = 2^(gamma2_t - gamma2_{16b+15}) for the blocks b below t's own
   float* Es = reinterpret_cast<float*>(smem + L::offTb);  // [4][16][LDE]
@@ -269,11 +293,29 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (tid < 2 * kChunk) {
       const float r = norm_qk ? tc::inv_norm(tc::row_sumsq_sw128<DK>(KQ, (tid & 63) + 64 * (tid >> 6))) : 1.f;
       rnk[tid] = r;  // tid 0..63: k rows, 64..127: q rows (rnq = rnk + 64)
-      if (norm_qk) ws_rn[((size_t)slot * Hk + hk) * (2 * kChunk) + tid] = r;  // for the state carry
+      if (norm_qk && !F16) ws_rn[((size_t)slot * Hk + hk) * (2 * kChunk) + tid] = r;  // for the state carry
     }
     if (!tc::mbar_wait(&bar[1], ph, 1u << 24)) atomicOr(err, 4);
     tc::fence_after();
-    __syncthreads();  // Grams done (they stay in TMEM) and norms visible; the tiles are dead from here on
+    __syncthreads();  // Grams done (they stay in TMEM) and norms visible
+
+    // ---- fp16 [K; Q] for the state carry: the tile's image, row by row scaled by its inverse
+    // norm (1 without normalisation).  bf16 values of magnitude 2^-17 .. 65504 are exact in fp16.
+    // Byte 16 e of the image lies in tile row (e / 8) % 128 wherever the swizzle puts it in the
+    // row, so the image is copied in order.  The tiles are dead after this (A and Tm go over them).
+    if constexpr (F16) {
+      unsigned char* dst = ws_kq + ((size_t)slot * Hk + hk) * kws_kq_bytes(DK);
+      for (int e = tid; e < kKBlocks * 1024; e += kPrepThreads) {
+        const float sc = rnk[(e >> 3) & 127];  // k rows 0..63, then q rows (rnq = rnk + 64)
+        const uint4 raw = *reinterpret_cast<const uint4*>(KQ + 16 * e);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          o4[p] = pack_f16(sc * __uint_as_float(w4[p] << 16), sc * __uint_as_float(w4[p] & 0xffff0000u));
+        *reinterpret_cast<uint4*>(dst + 16 * e) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+    }
 
 
     for (int gi = 0; gi < G; ++gi) {
@@ -326,7 +368,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
       __syncthreads();
 
-      // ---- A (fp32) and P (bf16) straight from the Grams in TMEM ------------------------
+      // ---- A (fp32) and P (16-bit) straight from the Grams in TMEM ---------------------
       // Warp w reads TMEM lanes 32 (w % 4) .. + 31 -- rows 0..63 of the Gram are K K^T (A),
       // rows 64..127 Q K^T (P) -- and columns 32 (w / 4) .. + 31, 16 at a time.  A row's
       // entries in a 16-column block are the Gram's times one factor per row and one per
@@ -370,12 +412,12 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             for (int p = 0; p < 4; ++p)
               *reinterpret_cast<float4*>(arow + 4 * p) = make_float4(o[4 * p], o[4 * p + 1], o[4 * p + 2], o[4 * p + 3]);
           } else {
-            __nv_bfloat16* prow = Ps + t * LDB + cb;
+            uint16_t* prow = Ps + t * LDB + cb;
 #pragma unroll
             for (int p = 0; p < 2; ++p)
               *reinterpret_cast<uint4*>(prow + 8 * p) =
-                  make_uint4(pack_bf16(o[8 * p], o[8 * p + 1]), pack_bf16(o[8 * p + 2], o[8 * p + 3]),
-                             pack_bf16(o[8 * p + 4], o[8 * p + 5]), pack_bf16(o[8 * p + 6], o[8 * p + 7]));
+                  make_uint4(pack16<F16>(o[8 * p], o[8 * p + 1]), pack16<F16>(o[8 * p + 2], o[8 * p + 3]),
+                             pack16<F16>(o[8 * p + 4], o[8 * p + 5]), pack16<F16>(o[8 * p + 6], o[8 * p + 7]));
           }
         }
       }
@@ -443,17 +485,17 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
       __syncthreads();
 
-      // ---- bf16 Tm: to shared (for PT) and to the workspace ---------------------
-      __nv_bfloat16* wsT = ws + ((size_t)slot * Hv + h) * (2 * kWsTileElems);
-      __nv_bfloat16* wsPT = wsT + kWsTileElems;
+      // ---- 16-bit Tm: to shared (for PT) and to the workspace ------------------
+      uint16_t* wsT = ws + ((size_t)slot * Hv + h) * (2 * kWsTileElems);
+      uint16_t* wsPT = wsT + kWsTileElems;
       for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
         const int r = e >> 3, p = e & 7;
         const float* src = Tms + r * LDF + 8 * p;
         uint4 v;
-        v.x = pack_bf16(src[0], src[1]);
-        v.y = pack_bf16(src[2], src[3]);
-        v.z = pack_bf16(src[4], src[5]);
-        v.w = pack_bf16(src[6], src[7]);
+        v.x = pack16<F16>(src[0], src[1]);
+        v.y = pack16<F16>(src[2], src[3]);
+        v.z = pack16<F16>(src[4], src[5]);
+        v.w = pack16<F16>(src[6], src[7]);
         *reinterpret_cast<uint4*>(Tmb + r * LDB + 8 * p) = v;
         *reinterpret_cast<uint4*>(wsT + r * kChunk + 8 * p) = v;
       }
@@ -487,8 +529,8 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
               if (p <= kk) {
                 uint32_t bb[4];
                 ldsm_x4_t(bb, Tmb + (16 * kk + 8 * (m & 1) + (lane & 7)) * LDB + 8 * (2 * p + (m >> 1)));
-                mma_bf16(acc[2 * pp], a, bb[0], bb[1]);
-                mma_bf16(acc[2 * pp + 1], a, bb[2], bb[3]);
+                mma16<F16>(acc[2 * pp], a, bb[0], bb[1]);
+                mma16<F16>(acc[2 * pp + 1], a, bb[2], bb[3]);
               }
             }
           }
@@ -500,9 +542,9 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int cc = 16 * (2 * (warp & 1) + pp) + 8 * hh + 2 * (lane & 3);
-            *reinterpret_cast<uint32_t*>(Ps + r0 * LDB + cc) = pack_bf16(acc[2 * pp + hh][0], acc[2 * pp + hh][1]);
+            *reinterpret_cast<uint32_t*>(Ps + r0 * LDB + cc) = pack16<F16>(acc[2 * pp + hh][0], acc[2 * pp + hh][1]);
             *reinterpret_cast<uint32_t*>(Ps + (r0 + 8) * LDB + cc) =
-                pack_bf16(acc[2 * pp + hh][2], acc[2 * pp + hh][3]);
+                pack16<F16>(acc[2 * pp + hh][2], acc[2 * pp + hh][3]);
           }
         }
       }
@@ -611,42 +653,13 @@ gdn_chunk_table_kernel(const int32_t* __restrict__ cu, int B, int T, int32_t* __
 }
 
 // ---- launchers -----------------------------------------------------------------
-namespace {
-PFN_cuTensorMapEncodeTiled_v12000 prep_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
-            cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-}  // namespace
-
-template <int DK>
-cudaError_t launch_prep(const void* q, const void* k, const float* g, const float* beta,
-                        const int32_t* cu, const int32_t* chunk_off, void* ws, float* ws_rn, int* err, int B, int T,
-                        int Hk, int Hv, int nslots, int nc_dense, int norm_qk, int hk_base, int hk_count,
-                        int c_begin, int c_count, int persistent, cudaStream_t st) {
+template <int DK, bool F16>
+cudaError_t launch_prep_fmt(const CUtensorMap& mk, const CUtensorMap& mq, const float* g, const float* beta,
+                            const int32_t* cu, const int32_t* chunk_off, void* ws, float* ws_rn, void* ws_kq, int* err,
+                            int B, int T, int Hk, int Hv, int nslots, int nc_dense, int norm_qk, int hk_base,
+                            int hk_count, int c_begin, int c_count, int persistent, cudaStream_t st) {
   using L = PrepSmem<DK>;
-  PFN_cuTensorMapEncodeTiled_v12000 enc = prep_map_encoder();
-  if (enc == nullptr) return cudaErrorNotSupported;
-  const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
-  const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)Hk, (cuuint64_t)(ttot > 0 ? ttot : 1)};
-  const cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)Hk * DK * 2};
-  const cuuint32_t box[3] = {64, 1, 64}, es[3] = {1, 1, 1};
-  CUtensorMap mk, mq;
-  if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-      enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_limit_once<gdn_prep_kernel<DK>>(L::bytes);
+  cudaError_t e = set_smem_limit_once<gdn_prep_kernel<DK, F16>>(L::bytes);
   if (e != cudaSuccess) return e;
   if (cu == nullptr && (c_begin < 0 || c_count <= 0 || c_begin + c_count > nc_dense)) return cudaErrorInvalidValue;
   // items: key heads hk_base .. hk_base + hk_count - 1 of B sequences x c_count chunks (dense)
@@ -666,18 +679,44 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const floa
   static_assert(kPrepCtasPerSm * (L::bytes + 1024) <= 228 * 1024, "the CTAs of an SM do not fit in shared memory");
   static std::atomic<bool> carved[64] = {};
   if (dev < 0 || dev >= 64 || !carved[dev].load(std::memory_order_acquire)) {
-    if ((e = cudaFuncSetAttribute(gdn_prep_kernel<DK>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    if ((e = cudaFuncSetAttribute(gdn_prep_kernel<DK, F16>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
       return e;
     if (dev >= 0 && dev < 64) carved[dev].store(true, std::memory_order_release);
   }
   const long long resident = (long long)sms * kPrepCtasPerSm;
   const long long grid = persistent && n_items > resident ? resident : n_items;
-  gdn_prep_kernel<DK><<<(unsigned)grid, kPrepThreads, L::bytes, st>>>(mk, mq, g, beta, cu, chunk_off,
-                                                           static_cast<__nv_bfloat16*>(ws), ws_rn, err, B, T, Hk, Hv,
-                                                           nc_dense, norm_qk, hk_base, hk_count, c_begin,
-                                                           c_count, (int)n_items);
+  gdn_prep_kernel<DK, F16><<<(unsigned)grid, kPrepThreads, L::bytes, st>>>(
+      mk, mq, g, beta, cu, chunk_off, static_cast<uint16_t*>(ws), ws_rn, static_cast<unsigned char*>(ws_kq), err, B,
+      T, Hk, Hv, nc_dense, norm_qk, hk_base, hk_count, c_begin, c_count, (int)n_items);
   return cudaGetLastError();
+}
+
+// f16: the fp16 outputs (and [K; Q] image in ws_kq) of the default state carry; 0: bf16 tiles.
+template <int DK>
+cudaError_t launch_prep(const void* q, const void* k, const float* g, const float* beta,
+                        const int32_t* cu, const int32_t* chunk_off, void* ws, float* ws_rn, void* ws_kq, int f16,
+                        int* err, int B, int T, int Hk, int Hv, int nslots, int nc_dense, int norm_qk, int hk_base,
+                        int hk_count, int c_begin, int c_count, int persistent, cudaStream_t st) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
+  const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)Hk, (cuuint64_t)(ttot > 0 ? ttot : 1)};
+  const cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)Hk * DK * 2};
+  const cuuint32_t box[3] = {64, 1, 64}, es[3] = {1, 1, 1};
+  CUtensorMap mk, mq;
+  if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (f16)
+    return launch_prep_fmt<DK, true>(mk, mq, g, beta, cu, chunk_off, ws, ws_rn, ws_kq, err, B, T, Hk, Hv, nslots,
+                                     nc_dense, norm_qk, hk_base, hk_count, c_begin, c_count, persistent, st);
+  return launch_prep_fmt<DK, false>(mk, mq, g, beta, cu, chunk_off, ws, ws_rn, ws_kq, err, B, T, Hk, Hv, nslots,
+                                    nc_dense, norm_qk, hk_base, hk_count, c_begin, c_count, persistent, st);
 }
 
 cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_off, int32_t* order, int* err,
@@ -688,8 +727,8 @@ cudaError_t launch_chunk_table(const int32_t* cu, int B, int T, int32_t* chunk_o
 
 #define GDN_INST_PREP(DK)                                                                                  \
   template cudaError_t launch_prep<DK>(const void*, const void*, const float*, const float*, const int32_t*, \
-                                       const int32_t*, void*, float*, int*, int, int, int, int, int, int, int,  \
-                                       int, int, int, int, int, cudaStream_t);
+                                       const int32_t*, void*, float*, void*, int, int*, int, int, int, int, int, \
+                                       int, int, int, int, int, int, int, cudaStream_t);
 GDN_INST_PREP(32)
 GDN_INST_PREP(64)
 GDN_INST_PREP(128)

@@ -8,7 +8,7 @@
 // or a caller that must not trigger the implicit device synchronisation that
 // cudaMalloc/cudaFree bring.  This entry point takes only the caller's inputs
 // and outputs and never allocates: its scratch (the chunk table and the per-chunk
-// Tm / PT tiles) lives in `g_static_scratch` below, which every GPU that loads
+// Tm / PT tiles, the fp16 k / q images) lives in `g_static_scratch` below, which every GPU that loads
 // the library holds until the process exits.
 //
 // Limits and sharing.  The array holds GDN_STATIC_SCRATCH_BYTES; a call whose
@@ -36,15 +36,14 @@
 namespace gdn {
 template <int DK>
 cudaError_t launch_prep(const void*, const void*, const float*, const float*, const int32_t*, const int32_t*,
-                        void*, float*, int*, int, int, int, int, int, int, int, int, int, int, int, int,
+                        void*, float*, void*, int, int*, int, int, int, int, int, int, int, int, int, int, int, int,
                         cudaStream_t);
 cudaError_t launch_chunk_table(const int32_t*, int, int, int32_t*, int32_t*, int*, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 template <int DK>
-cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*, const float*, const int32_t*,
-                            const int32_t*, const int32_t*, const void*, const float*, const float*, void*, float*,
-                            int*, int, int, int, int, int, int, long long, int, int, int, int, int, int,
-                            cudaStream_t);
+cudaError_t launch_chain_f16(const void*, const float*, const float*, const int32_t*, const int32_t*,
+                             const int32_t*, const void*, const void*, const float*, void*, float*, int*, int, int,
+                             int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
 }  // namespace gdn
 
 namespace {
@@ -99,12 +98,12 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   if (ntok == 0 && final_state == nullptr) return GDN_OK;
 
   // scratch layout: [256 B status words][chunk table and dispatch order][Tm/PT tiles]
-  //                 [inverse q/k norms per (slot, key head)]
+  //                 [inverse q/k norms per (slot, key head)][fp16 [K; Q] images per (slot, key head)]
   const long long nslots = packed ? (long long)(T + gdn::kChunk - 1) / gdn::kChunk + B
                                   : (long long)B * ((T + gdn::kChunk - 1) / gdn::kChunk);
   const size_t table = gdn::chunk_table_bytes(B);
   const size_t need = 256 + table + (size_t)nslots * Hv * gdn::kWsPerSlotHead +
-                      (size_t)nslots * Hk * gdn::kWsNormPerSlotKHead;
+                      (size_t)nslots * Hk * gdn::kWsNormPerSlotKHead + (size_t)nslots * Hk * gdn::kws_kq_bytes(dk);
   if (need > (size_t)GDN_STATIC_SCRATCH_BYTES || nslots > 0x7fffffffLL) return GDN_ERR_SCRATCH;
 
   int dev = 0;
@@ -120,6 +119,7 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   int32_t* order = packed ? chunk_off + B + 1 : nullptr;  // packed: state carries longest first
   void* tiles = static_cast<unsigned char*>(base) + 256 + table;
   float* ws_rn = reinterpret_cast<float*>(static_cast<unsigned char*>(tiles) + (size_t)nslots * Hv * gdn::kWsPerSlotHead);
+  void* ws_kq = reinterpret_cast<unsigned char*>(ws_rn) + (size_t)nslots * Hk * gdn::kWsNormPerSlotKHead;
   const int nc_dense = (T + gdn::kChunk - 1) / gdn::kChunk;
   if (packed) {
     e = gdn::launch_chunk_table(cu_seqlens, B, T, chunk_off, order, err, st);
@@ -131,17 +131,17 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   if (ev[0] != nullptr && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   if (nslots > 0) {
     switch (dk) {
-      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
-      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
-      default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
+      case 32: e = gdn::launch_prep<32>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, ws_kq, 1, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
+      case 64: e = gdn::launch_prep<64>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, ws_kq, 1, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
+      default: e = gdn::launch_prep<128>(q, k, g, beta, cu_seqlens, chunk_off, tiles, ws_rn, ws_kq, 1, err, B, T, Hk, Hv, (int)nslots, nc_dense, 0, 0, Hk, 0, nc_dense, 1, st); break;
     }
     if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   }
   if (ev[1] != nullptr && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   switch (dk) {
-    case 32: e = gdn::launch_chain_tc<32>(q, k, v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, 0, st); break;
-    case 64: e = gdn::launch_chain_tc<64>(q, k, v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, 0, st); break;
-    default: e = gdn::launch_chain_tc<128>(q, k, v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_rn, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, 0, Hv, 0, INT_MAX, 0, st); break;
+    case 32: e = gdn::launch_chain_f16<32>(v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_kq, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, Hv, 0, INT_MAX, 0, st); break;
+    case 64: e = gdn::launch_chain_f16<64>(v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_kq, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, Hv, 0, INT_MAX, 0, st); break;
+    default: e = gdn::launch_chain_f16<128>(v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_kq, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, Hv, 0, INT_MAX, 0, st); break;
   }
   if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);

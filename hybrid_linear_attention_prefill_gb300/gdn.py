@@ -24,17 +24,19 @@ GDN_ERR_ALIGN = -2
 GDN_ERR_ALLOC = -3
 GDN_ERR_LAUNCH = -4
 GDN_ERR_SCRATCH = -5
-GDN_STATIC_SCRATCH_BYTES = 64 << 20
+GDN_STATIC_SCRATCH_BYTES = 128 << 20
 GDN_FLAG_L2NORM_QK = 1
 GDN_FLAG_TWO_LEVEL = 2
 GDN_FLAG_ONE_LEVEL = 4
 GDN_FLAG_SLICE32 = 0x10000
 GDN_FLAG_SLICE16 = 0x40000
 GDN_FLAG_SLICE64 = 0x20000
+GDN_FLAG_WIDE_RANGE = 0x80000
 GDN_STATUS_MMA_TIMEOUT = 1
 GDN_STATUS_LOAD_TIMEOUT = 2
 GDN_STATUS_PREP_LOAD_TIMEOUT = 4
 GDN_STATUS_BAD_CU_SEQLENS = 8
+GDN_STATUS_NONFINITE_STATE = 16
 
 
 def GDN_FLAG_SEGMENTS(n: int) -> int:

@@ -31,7 +31,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 4
+#define GDN_ABI_VERSION 5
 
 /* Status codes (0 = success, negative = error). */
 #define GDN_OK 0
@@ -50,9 +50,10 @@ extern "C" {
 #define GDN_FLAG_SLICE32 0x10000u /* state carry: 32 state rows per CTA */
 #define GDN_FLAG_SLICE16 0x40000u /* state carry: 16 state rows per CTA */
 #define GDN_FLAG_SLICE64 0x20000u /* state carry: 64 state rows per CTA (dv a multiple of 64) */
+#define GDN_FLAG_WIDE_RANGE 0x80000u /* state carry on bf16 hi + lo operand pairs (fp32 range; slower) */
 
 /* Size of the fixed device scratch array behind gdn_prefill_static (64 MiB per device). */
-#define GDN_STATIC_SCRATCH_BYTES (64u << 20)
+#define GDN_STATIC_SCRATCH_BYTES (128u << 20)
 
 /* Returns GDN_ABI_VERSION of the loaded library. */
 int gdn_abi_version(void);
@@ -87,8 +88,18 @@ int gdn_last_cuda_error(void);
  * GDN_STATUS_BAD_CU_SEQLENS (see gdn_device_status).  Value head h reads key head
  * h / (Hv / Hk).  dk and dv must each be 32, 64 or 128.
  *
+ * Precision and range.  The chunk products run on the tensor cores with fp32
+ * accumulation and fp16 operands: k and q (converted from bf16, exact for
+ * magnitudes 2^-17 .. 65504), the chunk's UT transform and score product, and the
+ * state-side operands rounded from the fp32 state (2^-11 relative).  The state
+ * itself is carried in fp32.  Operands beyond fp16's range (about 65504: values of
+ * that size, or a state that grows to it) make the state non-finite, which sets
+ * GDN_STATUS_NONFINITE_STATE; gdn_prefill_ex with GDN_FLAG_WIDE_RANGE carries the
+ * state-side operands as bf16 hi + lo pairs instead (fp32 range, 2^-16, slower).
+ *
  * Memory.  The library keeps a per-device, grow-only workspace (allocated on the
- * first call that needs more; about 16 KB per 64-token chunk and value head).
+ * first call that needs more; about 16 KB per 64-token chunk and value head, plus
+ * 32 KB per chunk and key head for dk = 128, 16 KB for dk <= 64).
  * After a call at the largest size, later calls allocate nothing.  gdn_prefill,
  * gdn_prefill_ex and gdn_prefill_host calls on one device share that workspace
  * (and gdn_prefill_host's staging area): calls whose GPU work could overlap
@@ -164,8 +175,13 @@ int gdn_prefill_host(const void *q, const void *k, const void *v,
  * than those of 32-row CTAs (many sequences or heads), 16 when twice as many 32-row
  * CTAs would still fit one wave (few heads), else 32.  More than one of them, or
  * GDN_FLAG_SLICE64 with dv = 32, is GDN_ERR_ARG.
- * The results are the same for every width.  Everything else as
- * gdn_prefill.
+ * The results are the same for every width.
+ *
+ * GDN_FLAG_WIDE_RANGE: the state carry takes its state-side tensor-core operands as
+ * bf16 hi + lo pairs (fp32 range, ~2^-16 relative) and the chunk's UT transform and
+ * score product as bf16, instead of fp16 throughout.  For inputs or states beyond
+ * fp16's range (see "Precision and range" under gdn_prefill); slower.  Everything
+ * else as gdn_prefill.
  */
 int gdn_prefill_ex(const void *q, const void *k, const void *v,
                    const float *g, const float *beta,
@@ -233,9 +249,9 @@ void gdn_set_phase_events(void *ev_begin, void *ev_mid, void *ev_end);
  * loading the library holds until the process exits; it calls no allocator.
  *   - Returns GDN_ERR_SCRATCH, before launching anything, when the problem needs
  *     more scratch than that.  gdn_workspace_bytes gives the need: 16 KiB per
- *     (64-token chunk, value head) pair, 512 B per (chunk, key head) pair and a
- *     small table -- for example 32.5 MiB for one 4,096-token sequence with 32
- *     value heads over 16 key heads.
+ *     (64-token chunk, value head) pair, 32.5 KiB per (chunk, key head) pair for
+ *     dk = 128 (16.5 KiB for dk <= 64) and a small table -- for example 64.5 MiB for
+ *     one 4,096-token sequence with 32 value heads over 16 key heads.
  *   - All calls on a device share the array and it keeps the last call's contents.
  *     Calls whose GPU work overlaps (other streams, other host threads) race on it:
  *     the caller must order them.
@@ -265,6 +281,7 @@ int gdn_prefill_static(const void *q, const void *k, const void *v,
 #define GDN_STATUS_LOAD_TIMEOUT 2      /* the state-carry kernel gave up waiting for a tile load */
 #define GDN_STATUS_PREP_LOAD_TIMEOUT 4 /* the preparation kernel gave up waiting (tile load or Gram product) */
 #define GDN_STATUS_BAD_CU_SEQLENS 8    /* cu_seqlens was not 0 = cu[0] <= ... <= cu[B] = T (entries clamped) */
+#define GDN_STATUS_NONFINITE_STATE 16  /* a final state of the fp16 state carry was not finite (see gdn_prefill) */
 
 /*
  * gdn_device_status -- synchronise the current device, return the status bits

@@ -84,8 +84,10 @@ def test_host_entry_rejects_bad_arguments(lib):
 def test_workspace_bytes(lib):
     per = 2 * 64 * 64 * 2   # Tm + PT per (chunk slot, value head)
     norms = 2 * 64 * 4      # inverse q/k norms per (chunk slot, key head)
-    assert gdn.gdn_workspace_bytes(1, 4096, 16, 32, 128, 128, 0) == 512 + 64 * 32 * per + 64 * 16 * norms
-    assert gdn.gdn_workspace_bytes(2, 100, 1, 1, 32, 32, 1) == 512 + (2 + 2) * (per + norms)
+    kq128, kq64 = 2 * 16384, 16384  # fp16 [K; Q] image per (chunk slot, key head), by dk
+    assert gdn.gdn_workspace_bytes(1, 4096, 16, 32, 128, 128, 0) == 512 + 64 * 32 * per + 64 * 16 * (norms + kq128)
+    assert gdn.gdn_workspace_bytes(2, 100, 1, 1, 32, 32, 1) == 512 + (2 + 2) * (per + norms + kq64)
+    assert gdn.gdn_workspace_bytes(1, 64, 1, 1, 64, 32, 0) == 512 + per + norms + kq64
     assert gdn.gdn_workspace_bytes(1, 10, 2, 3, 128, 128, 0) == 0
 
 
@@ -117,7 +119,7 @@ def test_decode_argument_checks(lib):
 def test_prefill_ex_rejects_unknown_flags(lib):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, cu_seqlens=None, init_state=None,
              out=FAKE, final_state=None, B=1, T=64, Hk=1, Hv=1, dk=128, dv=128, stream=0)
-    for bad in (8, 1 << 19, 1 << 31, gdn.GDN_FLAG_TWO_LEVEL | gdn.GDN_FLAG_ONE_LEVEL,
+    for bad in (8, 1 << 20, 1 << 31, gdn.GDN_FLAG_TWO_LEVEL | gdn.GDN_FLAG_ONE_LEVEL,
                 gdn.GDN_FLAG_SLICE32 | gdn.GDN_FLAG_SLICE64, gdn.GDN_FLAG_SLICE16 | gdn.GDN_FLAG_SLICE32,
                 gdn.GDN_FLAG_SLICE16 | gdn.GDN_FLAG_SLICE64):
         assert gdn.gdn_prefill_ex(**a, flags=bad) == gdn.GDN_ERR_ARG
@@ -125,7 +127,8 @@ def test_prefill_ex_rejects_unknown_flags(lib):
     assert gdn.gdn_prefill_ex(**{**a, "dk": 32, "dv": 32}, flags=gdn.GDN_FLAG_SLICE64) == gdn.GDN_ERR_ARG
     for ok in (gdn.GDN_FLAG_L2NORM_QK, gdn.GDN_FLAG_TWO_LEVEL | gdn.GDN_FLAG_SEGMENTS(5), gdn.GDN_FLAG_ONE_LEVEL,
                gdn.GDN_FLAG_SLICE16, gdn.GDN_FLAG_SLICE32, gdn.GDN_FLAG_SLICE64,
-               gdn.GDN_FLAG_SLICE64 | gdn.GDN_FLAG_L2NORM_QK):
+               gdn.GDN_FLAG_SLICE64 | gdn.GDN_FLAG_L2NORM_QK, gdn.GDN_FLAG_WIDE_RANGE,
+               gdn.GDN_FLAG_WIDE_RANGE | gdn.GDN_FLAG_SLICE16 | gdn.GDN_FLAG_L2NORM_QK):
         assert gdn.gdn_prefill_ex(**{**a, "B": 0}, flags=ok) == gdn.GDN_OK
 
 
@@ -138,6 +141,9 @@ def test_segment_flag_encoding():
     assert "#define GDN_FLAG_SLICE32 0x10000u" in hdr and "#define GDN_FLAG_SLICE64 0x20000u" in hdr
     assert "#define GDN_FLAG_SLICE16 0x40000u" in hdr
     assert (gdn.GDN_FLAG_SLICE16, gdn.GDN_FLAG_SLICE32, gdn.GDN_FLAG_SLICE64) == (0x40000, 0x10000, 0x20000)
+    assert "#define GDN_FLAG_WIDE_RANGE 0x80000u" in hdr and gdn.GDN_FLAG_WIDE_RANGE == 0x80000
+    assert "#define GDN_STATUS_NONFINITE_STATE 16" in hdr and gdn.GDN_STATUS_NONFINITE_STATE == 16
+    assert "#define GDN_STATIC_SCRATCH_BYTES (128u << 20)" in hdr and gdn.GDN_STATIC_SCRATCH_BYTES == 128 << 20
 
 
 def test_allocation_failure_hook_counts_down(lib):

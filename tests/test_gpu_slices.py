@@ -1,8 +1,10 @@
 """State-carry CTAs of 16, 32 or 64 state rows (GDN_FLAG_SLICE16 / 32 / 64) against the oracle,
-and against each other bit for bit (GPU).  The library takes 64 rows on its own for grids of many
-waves (the packed 32-candidate workload's parity test runs that way) and 16 for few heads (most
-small parity cases); these force each width on small inputs: dense and packed batches, every dk
-with dv = 32, 64 and 128, an initial state, many chunks, in-kernel q/k normalisation."""
+and against each other bit for bit (GPU), for both operand formats: the default fp16 state carry
+and the wide-range bf16 hi / lo one (GDN_FLAG_WIDE_RANGE).  The library takes 64 rows on its own
+for grids of many waves (the packed 32-candidate workload's parity test runs that way) and 16 for
+few heads (most small parity cases); these force each width on small inputs: dense and packed
+batches, every dk with dv = 32, 64 and 128, an initial state, many chunks, in-kernel q/k
+normalisation."""
 
 import numpy as np
 import pytest
@@ -40,20 +42,22 @@ def _both_widths_against_oracle(gdn, inp, extra=0, ref=None):
     import oracle
 
     o_ref, s_ref = ref if ref is not None else oracle.prefill_inputs(inp)
-    res = {}
     widths = [("16", gdn.GDN_FLAG_SLICE16), ("32", gdn.GDN_FLAG_SLICE32)]
     if inp.dv % 64 == 0:
         widths.append(("64", gdn.GDN_FLAG_SLICE64))
-    for name, flag in widths:
-        o, s = _run(gdn, inp, flag | extra)
-        eo, es = out_err(o, o_ref), state_err(s, s_ref)
-        print(f"\n[slices] {inp.name or 'case'} rows {name}: out {eo:.3e} state {es:.3e}")
-        assert np.all(np.isfinite(o)) and np.all(np.isfinite(s))
-        assert eo <= OUT_TOL and es <= STATE_TOL, (name, eo, es)
-        res[name] = (o, s)
-    # every width forms each column's products in the same order: bit for bit the same
-    for name in res:
-        assert np.array_equal(res["32"][0], res[name][0]) and np.array_equal(res["32"][1], res[name][1]), name
+    for fmt_name, fmt in (("fp16", 0), ("wide", gdn.GDN_FLAG_WIDE_RANGE)):
+        res = {}
+        for name, flag in widths:
+            o, s = _run(gdn, inp, flag | fmt | extra)
+            eo, es = out_err(o, o_ref), state_err(s, s_ref)
+            print(f"\n[slices] {inp.name or 'case'} {fmt_name} rows {name}: out {eo:.3e} state {es:.3e}")
+            assert np.all(np.isfinite(o)) and np.all(np.isfinite(s))
+            assert eo <= OUT_TOL and es <= STATE_TOL, (fmt_name, name, eo, es)
+            res[name] = (o, s)
+        # every width forms each column's products in the same order: bit for bit the same
+        for name in res:
+            assert np.array_equal(res["32"][0], res[name][0]) and np.array_equal(res["32"][1], res[name][1]), \
+                (fmt_name, name)
 
 
 @pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (32, 64), (128, 64), (64, 128), (128, 32), (32, 32)])

@@ -5,14 +5,16 @@ the kernel returns.  Here a wait is made to run out on purpose (an mbarrier that
 nothing completes), the host reads the bit, and the context is still usable --
 also for the status word of the allocation-free entry point.  A malformed
 cu_seqlens is reported the same way, and a workspace allocation that fails (made
-to fail on the host) returns GDN_ERR_ALLOC before anything is launched.
+to fail on the host) returns GDN_ERR_ALLOC before anything is launched.  Values
+beyond the fp16 operands' range make the default state carry's state non-finite,
+which its status bit reports; the wide-range state carry takes them.
 """
 
 import numpy as np
 import pytest
 
 from gpu_common import OUT_TOL, STATE_TOL, out_err, run_gpu, state_err
-from hybrid_linear_attention_prefill_gb300.inputs import make_gdn_inputs
+from hybrid_linear_attention_prefill_gb300.inputs import f32_to_bf16_bits, make_gdn_inputs
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -105,3 +107,27 @@ def test_malformed_cu_seqlens_sets_its_status_bit(gdn):
         assert np.all(np.isfinite(s))
         rc, bits = gdn.gdn_device_status()
         assert rc == gdn.GDN_OK and bits == gdn.GDN_STATUS_BAD_CU_SEQLENS, bad
+
+
+def test_values_beyond_fp16_range_are_reported_and_the_wide_range_carry_takes_them(gdn):
+    import oracle
+
+    from gpu_common import dev_inputs
+
+    inp = make_gdn_inputs(lengths=[130, 70], Hk=1, Hv=2, dk=128, dv=128, seed=84, init_std=0.1)
+    inp.v = f32_to_bf16_bits((inp.v64() * 1.0e5).astype(np.float32))  # values of order 1e5
+    gdn.gdn_device_status()
+    run_gpu(inp)
+    rc, bits = gdn.gdn_device_status()
+    assert rc == gdn.GDN_OK and bits == gdn.GDN_STATUS_NONFINITE_STATE
+    d = dev_inputs(inp)
+    out = torch.full((inp.total_tokens, inp.Hv, inp.dv), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fin = torch.full((inp.B, inp.Hv, inp.dv, inp.dk), float("nan"), device="cuda")
+    gdn.check(gdn.gdn_prefill_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], d["init"], out, fin,
+                                 inp.B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, gdn.GDN_FLAG_WIDE_RANGE))
+    torch.cuda.synchronize()
+    rc, bits = gdn.gdn_device_status()
+    assert rc == gdn.GDN_OK and bits == 0
+    o_ref, s_ref = oracle.prefill_inputs(inp)
+    o, s = out.float().cpu().numpy(), fin.cpu().numpy()
+    assert out_err(o, o_ref) <= OUT_TOL and state_err(s, s_ref) <= STATE_TOL

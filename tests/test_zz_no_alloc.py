@@ -62,9 +62,9 @@ def test_two_calls_match_gdn_prefill(gdn):
 
 
 def test_too_large_is_refused(gdn):
-    # 4,096 chunks of one value head need 64 MiB of tiles plus the table: one pair too
-    # many.  The buffers are the size the call claims, so even a refusal that went wrong
-    # could not read or write past them.
+    # 4,096 chunks of one head need 48.5 KiB each (Tm / PT tiles, the fp16 k / q image and
+    # the norms), 194 MiB in all, more than the 128 MiB array.  The buffers are the size the
+    # call claims, so even a refusal that went wrong could not read or write past them.
     T_big = 4096 * 64
     need = gdn.gdn_workspace_bytes(1, T_big, 1, 1, 128, 128, 0)
     assert need > gdn.GDN_STATIC_SCRATCH_BYTES
