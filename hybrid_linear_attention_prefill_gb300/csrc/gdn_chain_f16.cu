@@ -49,7 +49,7 @@ namespace {
 
 constexpr int kThreads = 288;  // 8 epilogue warps + 1 issue warp
 constexpr int kEpiThreads = 256;
-constexpr int kParts = 2;  // accumulators in phase 1 (K = dk); phases 2 and 3 use one
+constexpr int kParts = 1;  // TMEM accumulators per phase (two in phase 1 measured 2 % slower)
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr int kStatusNonFinite = 16;
 
@@ -57,7 +57,7 @@ template <int DVT>
 struct CfgH {
   static constexpr int kN = DVT;                       // MMA N: one fp16 column per state row
   static constexpr int kPS = kN < 32 ? 32 : kN;        // TMEM columns between phase 1's partials
-  static constexpr uint32_t kTmemCols = kParts * kPS;  // 64, 64, 128
+  static constexpr uint32_t kTmemCols = kParts * kPS;  // 32, 32, 64
   static constexpr int kCPT = DVT / 2;                 // state columns per epilogue thread
   static constexpr int kGW = kCPT < 16 ? kCPT : 16;    // columns an epilogue step works on
   static constexpr int kNG = kCPT / kGW;               // steps per thread
@@ -298,6 +298,13 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
   cp_async_commit();
 
   const int tok = 32 * (q4 & 1) + lane;  // this thread's token in phases 1-2
+  // shared-memory descriptors of the operands at stage 0 / their buffers (the issuer's MMAs)
+  const uint64_t dKQ0 = tc::sdesc(sb + C::kOffKQ, 16, 1024, tc::kSw128);     // [K; Q], K-major
+  const uint64_t dKT0 = tc::sdesc(sb + C::kOffKQ, 16384, 1024, tc::kSw128);  // K^T, MN-major
+  const uint64_t dTP0 = tc::sdesc(sb + C::kOffTP, 16, 1024, tc::kSw128);     // [Tm; PT], K-major
+  const uint64_t dS = tc::sdesc(sb + C::kOffS, 16384, 1024, tc::kSw128);     // S, MN-major
+  const uint64_t dR = tc::sdesc(sb + C::kOffR, 8192, 1024, tc::kSw128);      // R, MN-major
+  const uint64_t dU = tc::sdesc(sb + C::kOffU, 8192, 1024, tc::kSw128);      // dU, MN-major
   bool aborted = false;
   int c = c0;
   for (; c < c1; ++c) {
@@ -305,20 +312,24 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     const int stg = ci % C::kStages;
     const uint32_t par = (uint32_t)(ci & 1);
     unsigned char* st = sm + stg * C::kStage;
-    const uint32_t st_s = sb + stg * C::kStage;
     cp_async_wait<0>();
     if (!tc::mbar_wait(&full[stg], (uint32_t)((ci / C::kStages) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
     __syncthreads();
     if (*abort_flag) { aborted = true; break; }
 
     if (issuer) {
+      // Descriptors: this stage's bases plus each MMA's offset, added to the start-address field
+      // (byte offset / 16; shared addresses stay below 2^18, so the 14-bit field does not carry).
+      const uint64_t dKQ = dKQ0 + (uint64_t)((uint32_t)(stg * C::kStage) >> 4);
+      const uint64_t dKT = dKT0 + (uint64_t)((uint32_t)(stg * C::kStage) >> 4);
+      const uint64_t dTP = dTP0 + (uint64_t)((uint32_t)(stg * C::kStage) >> 4);
       // ---- phase 1: [X; Y] = [K; Q] S^T --------------------------------------------
       if (lane == 0) {
         tc::fence_after();
 #pragma unroll
         for (int ks = 0; ks < DK / 16; ++ks) {
-          const uint64_t a = tc::sdesc(st_s + C::kOffKQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSw128);
-          const uint64_t bd = tc::sdesc(sb + C::kOffS + ks * 2048, 16384, 1024, tc::kSw128);
+          const uint64_t a = dKQ + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
+          const uint64_t bd = dS + (uint64_t)((ks * 2048) >> 4);
           tc::mma_bf16(tmem + C::kPS * (ks % kP1), a, bd, C::kID_KS, ks >= kP1);
         }
         tc::commit(&bars[0]);
@@ -333,11 +344,8 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
       if (lane == 0) {
         tc::fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = tc::sdesc(st_s + C::kOffTP + ks * 32, 16, 1024, tc::kSw128);
-          const uint64_t bd = tc::sdesc(sb + C::kOffR + ks * 2048, 8192, 1024, tc::kSw128);
-          tc::mma_bf16(tmem, a, bd, C::kID_KS, ks > 0);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem, dTP + (uint64_t)((ks * 32) >> 4), dR + (uint64_t)((ks * 2048) >> 4), C::kID_KS, ks > 0);
         tc::commit(&bars[1]);
       }
       __syncwarp();
@@ -347,11 +355,8 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
       if (lane == 0) {
         tc::fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = tc::sdesc(st_s + C::kOffKQ + ks * 2048, 16384, 1024, tc::kSw128);
-          const uint64_t bd = tc::sdesc(sb + C::kOffU + ks * 2048, 8192, 1024, tc::kSw128);
-          tc::mma_bf16(tmem, a, bd, C::kID_KT, ks > 0);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem, dKT + (uint64_t)((ks * 2048) >> 4), dU + (uint64_t)((ks * 2048) >> 4), C::kID_KT, ks > 0);
         tc::commit(&bars[2]);
       }
       __syncwarp();
@@ -543,10 +548,11 @@ cudaError_t launch_chain_f16_dvt(const void* v, const CUtensorMap& mw, const voi
 }
 
 // slice: state rows per CTA, 16, 32 or 64, or 0 for the library's choice.  The MMA issue and
-// the hand-offs of a chunk step do not depend on the width and its epilogues scale with it.
-// So 64 rows when dv allows it and 1.5 x its waves of one CTA per SM are fewer than the 32-row
-// grid's waves (many sequences or heads); 16 rows when twice the 32-row grid still fits one
-// wave (few heads: the chain latency decides, and narrower slices shorten it); 32 otherwise.
+// the hand-offs of a chunk step do not depend on the width and its epilogues scale with it:
+// measured at 64 chunks, a 16-row step takes 0.91x a 32-row one and a 64-row step 1.41x.  So 64
+// rows when dv allows it and 1.41 x its waves of one CTA per SM are fewer than the 32-row grid's
+// waves (many sequences or heads); 16 rows when twice the 32-row grid still fits one wave (few
+// heads: the chain latency decides, and narrower slices shorten it); 32 otherwise.
 template <int DK>
 cudaError_t launch_chain_f16(const void* v, const float* g, const float* beta, const int32_t* cu,
                              const int32_t* chunk_off, const int32_t* order, const void* ws, const void* ws_kq,
@@ -573,7 +579,7 @@ cudaError_t launch_chain_f16(const void* v, const float* g, const float* beta, c
       return e;
     const long long n32 = (long long)B * (DV / 32) * h_count;
     const long long waves32 = (n32 + sms - 1) / sms, waves64 = (n32 / 2 + sms - 1) / sms;
-    if (DV % 64 == 0 && 3 * waves64 < 2 * waves32) slice = 64;
+    if (DV % 64 == 0 && 141 * waves64 < 100 * waves32) slice = 64;
     else if (2 * n32 <= sms) slice = 16;
   }
   switch (slice) {
