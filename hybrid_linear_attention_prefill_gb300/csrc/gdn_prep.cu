@@ -250,12 +250,34 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   // Persistent CTAs (as many per SM as fit) walk the items with the grid's stride.  While one item is
   // worked on, the next one's key and query tiles are brought into L2, so its tile copy
   // does not wait for DRAM.
+  int cur_slot = 0, cur_hk = 0;  // the item write_kq_image writes
+  // ---- fp16 [K; Q] for the state carry: the tile's image, row by row scaled by its inverse
+  // norm when q and k are normalised in-kernel.  bf16 values of magnitude 2^-17 .. 65504 are
+  // exact in fp16.  Byte 16 e of the image lies in tile row (e / 8) % 128 wherever the swizzle
+  // puts it in the row, so the image is copied in order.
+  auto write_kq_image = [&](bool scaled) {
+    if constexpr (F16) {
+      unsigned char* dst = ws_kq + ((size_t)cur_slot * Hk + cur_hk) * kws_kq_bytes(DK);
+      for (int e = tid; e < kKBlocks * 1024; e += kPrepThreads) {
+        const float sc = scaled ? rnk[(e >> 3) & 127] : 1.f;  // k rows 0..63, then q rows (rnq = rnk + 64)
+        const uint4 raw = *reinterpret_cast<const uint4*>(KQ + 16 * e);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          o4[p] = pack_f16(sc * __uint_as_float(w4[p] << 16), sc * __uint_as_float(w4[p] & 0xffff0000u));
+        *reinterpret_cast<uint4*>(dst + 16 * e) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+    }
+  };
   uint32_t ph = 0;  // phase of bar[0] and bar[1]: each completes once per item worked on
   int ahead = -1;   // (thread 0) the item whose tiles went out while the one before it was worked on
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     Item cur;
     if (!locate(item, cur)) continue;  // the same for every thread of the CTA
     const int slot = cur.slot, hk = cur.hk, n = cur.n;
+    cur_slot = slot;
+    cur_hk = hk;
 
     // the loads of this item (the first item's went out before the set-up barrier)
     if (item != (int)blockIdx.x) {
@@ -295,28 +317,14 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       rnk[tid] = r;  // tid 0..63: k rows, 64..127: q rows (rnq = rnk + 64)
       if (norm_qk && !F16) ws_rn[((size_t)slot * Hk + hk) * (2 * kChunk) + tid] = r;  // for the state carry
     }
+    // without normalisation the image needs no norms: written while the product runs (the
+    // tensor core only reads the tile)
+    if (F16 && !norm_qk) write_kq_image(false);
     if (!tc::mbar_wait(&bar[1], ph, 1u << 24)) atomicOr(err, 4);
     tc::fence_after();
-    __syncthreads();  // Grams done (they stay in TMEM) and norms visible
+    __syncthreads();  // Grams done (they stay in TMEM) and norms visible; the tiles are dead after the image
 
-    // ---- fp16 [K; Q] for the state carry: the tile's image, row by row scaled by its inverse
-    // norm (1 without normalisation).  bf16 values of magnitude 2^-17 .. 65504 are exact in fp16.
-    // Byte 16 e of the image lies in tile row (e / 8) % 128 wherever the swizzle puts it in the
-    // row, so the image is copied in order.  The tiles are dead after this (A and Tm go over them).
-    if constexpr (F16) {
-      unsigned char* dst = ws_kq + ((size_t)slot * Hk + hk) * kws_kq_bytes(DK);
-      for (int e = tid; e < kKBlocks * 1024; e += kPrepThreads) {
-        const float sc = rnk[(e >> 3) & 127];  // k rows 0..63, then q rows (rnq = rnk + 64)
-        const uint4 raw = *reinterpret_cast<const uint4*>(KQ + 16 * e);
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t o4[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-          o4[p] = pack_f16(sc * __uint_as_float(w4[p] << 16), sc * __uint_as_float(w4[p] & 0xffff0000u));
-        *reinterpret_cast<uint4*>(dst + 16 * e) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-      }
-    }
-
+    if (F16 && norm_qk) write_kq_image(true);  // scaled by the norms just summed
 
     for (int gi = 0; gi < G; ++gi) {
       const int h = hk * G + gi;
