@@ -333,46 +333,41 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       __syncthreads();
       if (gi + 1 < G) load_gb(cur, gi + 1, (gi + 1) & 1);
       // ---- gamma = inclusive cumsum of g in the chunk, in log2 units -------------------
-      // Every warp scans the 64 values in registers (lane l holds tokens l and l + 32), so
-      // no warp waits for another; the A/P build below takes its entries by shuffle.
-      const float* gb = gbuf + (gi & 1) * 2 * kChunk;  // [g 64 | beta 64]
-      float gl0 = gb[lane], gl1 = gb[lane + 32];
+      // Warp 0 scans the 64 values once (lane l: tokens 2l and 2l + 1, then a five-step warp
+      // scan of the pair sums) and writes gamma2 over this head's g, which nothing reads
+      // afterwards; every thread then takes the entries it needs from shared memory.
+      float* gb = gbuf + (gi & 1) * 2 * kChunk;  // [g 64 | beta 64]; g becomes gamma2
+      if (warp == 0) {
+        const float2 gg = *reinterpret_cast<const float2*>(gb + 2 * lane);
+        const float pair = gg.x + gg.y;
+        float incl = pair;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u0 = __shfl_up_sync(0xffffffffu, gl0, o);
-        const float u1 = __shfl_up_sync(0xffffffffu, gl1, o);
-        if (lane >= o) { gl0 += u0; gl1 += u1; }
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        const float excl = incl - pair;
+        *reinterpret_cast<float2*>(gb + 2 * lane) =
+            make_float2((excl + gg.x) * 1.4426950408889634f, incl * 1.4426950408889634f);  // log2(e)
       }
-      gl1 += __shfl_sync(0xffffffffu, gl0, 31);
-      gl0 *= 1.4426950408889634f;  // log2(e)
-      gl1 *= 1.4426950408889634f;
+      __syncthreads();
+      const float* g2 = gb;  // gamma2 of the chunk's tokens
 
       // ---- the decay tables of this value head (every thread) ----------------------------
       // Gamma[t][i] = 2^(gamma2_t - gamma2_i), i <= t, with every exponent <= 0: inside a
       // 16 x 16 diagonal block from the table Es, below it as the product of a row factor
       // (to the block's last column j0) and a column factor (from j0), both <= 1.
       {
-        // gamma2 of token x: lane x % 32 holds it in gl0 (x < 32) or gl1; where the half is
-        // the same for the whole warp, one shuffle fetches it
-        auto g2u = [&](bool upper, int x) { return __shfl_sync(0xffffffffu, upper ? gl1 : gl0, x & 31); };
         static_assert(kPrepThreads == 256, "one table row block per 256 entries");
         const int r = (tid >> 4) & 15, c = tid & 15;
 #pragma unroll
-        for (int bl = 0; bl < 4; ++bl) {  // Es[bl][r][c], the block's half of the tokens known at compile time
-          const float gr = g2u(bl >= 2, 16 * bl + r), gc = g2u(bl >= 2, 16 * bl + c);
-          Es[(16 * bl + r) * LDE + c] = c <= r ? exp2f(gr - gc) * rnk[16 * bl + c] : 0.f;
-        }
+        for (int bl = 0; bl < 4; ++bl)  // Es[bl][r][c]
+          Es[(16 * bl + r) * LDE + c] = c <= r ? exp2f(g2[16 * bl + r] - g2[16 * bl + c]) * rnk[16 * bl + c] : 0.f;
         {
-          const int t = tid >> 2, bl = tid & 3;  // t < 32 for warps 0..3
-          const float gt = g2u(tid >= 128, t);
-          const float j0 = __shfl_sync(0xffffffffu, gl0, (16 * bl + 15) & 31);
-          const float j1 = __shfl_sync(0xffffffffu, gl1, (16 * bl + 15) & 31);
-          rfs[tid] = bl < (t >> 4) ? exp2f(gt - (bl < 2 ? j0 : j1)) : 0.f;
+          const int t = tid >> 2, bl = tid & 3;
+          rfs[tid] = bl < (t >> 4) ? exp2f(g2[t] - g2[16 * bl + 15]) : 0.f;
         }
-        if (tid < kChunk) {  // warps 0 and 1: tokens tid
-          const float gi = tid < 32 ? gl0 : gl1, gj = g2u(tid >= 32, tid | 15);
-          cfs[tid] = rnk[tid] * exp2f(gj - gi);
-        }
+        if (tid < kChunk) cfs[tid] = rnk[tid] * exp2f(g2[tid | 15] - g2[tid]);  // warps 0 and 1: tokens tid
       }
       __syncthreads();
 
