@@ -396,6 +396,9 @@ def run_gpu_arm(args):
             "steps": K, "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(args, inp, world),
+            # bf16 inputs and outputs; the chunk products on the tensor cores take fp16 operands and
+            # accumulate in fp32; the state is carried in fp32
+            "arith": {"io": "bf16", "products": "fp16 x fp16 -> fp32 (tcgen05)", "state": "fp32"},
             "roofline": roofline, "path_roofline": path_roof,
             "kernels_us": {k: round(v * 1e3, 2) for k, v in kernels.items()},
             "ms_per_step_min": min(step_ms), "ms_per_step_median": statistics.median(step_ms),
