@@ -176,6 +176,15 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                      const int32_t* __restrict__ chunk_off, const int32_t* __restrict__ order, const float* init,
                      __nv_bfloat16* __restrict__ out, float* fin, int* __restrict__ err, int B, int T, int Hk,
                      int Hv, int DV, int nc_dense, long long nslots, int h_base, int c_begin, int c_end) {
+  // The value tiles are inputs, ready before the preparation kernel finishes: for dense batches
+  // the issue thread brings the first chunks' tiles into L2 before the wait below.
+  if (cu == nullptr && threadIdx.x == 256) {
+    const int nt = DV / DVT;
+    const int bb = (int)blockIdx.x / nt, d0 = ((int)blockIdx.x - bb * nt) * DVT, hh = h_base + (int)blockIdx.y;
+    tc::prefetch_tensormap(&tm_v);
+    for (int cc = c_begin; cc < c_begin + CfgH<DVT>::kStages && cc * kChunk < T; ++cc)
+      tc::tma_prefetch_l2_3d(&tm_v, d0, hh, (int)((long long)bb * T + (long long)cc * kChunk));
+  }
   // Launched as a programmatic dependent of the kernel before it in the stream (the preparation
   // kernel): the CTA starts while that kernel's last CTAs run and waits here until it has
   // completed and its writes are visible (otherwise this returns at once).
