@@ -29,7 +29,7 @@ cudaError_t launch_chain_tc(const void*, const void*, const void*, const float*,
 template <int DK>
 cudaError_t launch_chain_f16(const void*, const float*, const float*, const int32_t*, const int32_t*,
                              const int32_t*, const void*, const void*, const float*, void*, float*, int*, int, int,
-                             int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
+                             int, int, int, int, long long, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t st);
 cudaError_t launch_seg_setup(const float*, float*, float*, int32_t*, int32_t*, int, int, int, int, int, int, int,
                              cudaStream_t);
@@ -216,29 +216,31 @@ int prepare_scan(int dev, int B, int T, int Hv, int dk, int dv, bool packed, uns
 }
 
 // The state carry of value heads [h_base, h_base + h_count): fp16 operands by default, bf16
-// hi / lo pairs when `wide` (then with q and k read from the inputs).
+// hi / lo pairs when `wide` (then with q and k read from the inputs).  check_small: the fp16
+// kernel reports a final state below its accurate range (off for the two-level scan's runs).
 template <int DK>
 cudaError_t carry(int wide, const void* q, const void* k, const void* v, const float* g, const float* beta,
                   const int32_t* cu, const int32_t* chunk_off, const int32_t* order, const void* tiles,
                   const float* ws_rn, const void* ws_kq, const float* init, void* out, float* fin, int* err, int B,
                   int T, int Hk, int Hv, int DV, int nc_dense, long long nslots, int norm_qk, int h_base,
-                  int h_count, int c_begin, int c_end, int slice, cudaStream_t st) {
+                  int h_count, int c_begin, int c_end, int slice, int check_small, cudaStream_t st) {
   if (wide)
     return gdn::launch_chain_tc<DK>(q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, init, out, fin, err, B, T,
                                     Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, st);
   return gdn::launch_chain_f16<DK>(v, g, beta, cu, chunk_off, order, tiles, ws_kq, init, out, fin, err, B, T, Hk,
-                                   Hv, DV, nc_dense, nslots, h_base, h_count, c_begin, c_end, slice, st);
+                                   Hv, DV, nc_dense, nslots, h_base, h_count, c_begin, c_end, slice, check_small, st);
 }
 
 cudaError_t carry_dk(int dk, int wide, const void* q, const void* k, const void* v, const float* g,
                      const float* beta, const int32_t* cu, const int32_t* chunk_off, const int32_t* order,
                      const void* tiles, const float* ws_rn, const void* ws_kq, const float* init, void* out,
                      float* fin, int* err, int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots,
-                     int norm_qk, int h_base, int h_count, int c_begin, int c_end, int slice, cudaStream_t st) {
+                     int norm_qk, int h_base, int h_count, int c_begin, int c_end, int slice, int check_small,
+                     cudaStream_t st) {
   switch (dk) {
-    case 32: return carry<32>(wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, st);
-    case 64: return carry<64>(wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, st);
-    default: return carry<128>(wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, st);
+    case 32: return carry<32>(wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, check_small, st);
+    case 64: return carry<64>(wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, check_small, st);
+    default: return carry<128>(wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk, Hv, DV, nc_dense, nslots, norm_qk, h_base, h_count, c_begin, c_end, slice, check_small, st);
   }
 }
 
@@ -251,7 +253,7 @@ cudaError_t chain_dk(int dk, int wide, const void* q, const void* k, const void*
                      int B, int T, int Hk, int Hv, int DV, int nc_dense, long long nslots, int norm_qk,
                      cudaStream_t st) {
   return carry_dk(dk, wide, q, k, v, g, beta, cu, chunk_off, nullptr, tiles, ws_rn, ws_kq, init, out, fin, err, B, T,
-                  Hk, Hv, DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, 32, st);
+                  Hk, Hv, DV, nc_dense, nslots, norm_qk, 0, Hv, 0, INT_MAX, 32, 0, st);
 }
 
 // The prefill for value heads [h0, h1) (all heads when h1 < 0; h0 and h1 multiples of
@@ -362,7 +364,7 @@ int launch_all(const void* q, const void* k, const void* v, const float* g, cons
     return GDN_OK;
   }
   e = carry_dk(dk, wide, q, k, v, g, beta, cu, chunk_off, order, tiles, ws_rn, ws_kq, init, out, fin, err, B, T, Hk,
-               Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, slice, st);
+               Hv, dv, nc_dense, nslots, norm_qk, h0, h1 - h0, cc0, cc1, slice, 1, st);
   if (e != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return set_cuda_error(e, GDN_ERR_LAUNCH);
   return GDN_OK;

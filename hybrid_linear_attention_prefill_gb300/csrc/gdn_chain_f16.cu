@@ -27,7 +27,10 @@
 // largest, on a no-decay, beta = 0.999 stress case): bf16 Tm was their largest rounding.
 // fp16 stops at 65504.  An operand beyond it becomes infinite, and that reaches the state, so
 // a (sequence, head) whose final fp32 state is not finite sets status bit 16 (also for
-// non-finite inputs); the wide-range kernel takes values of any magnitude.
+// non-finite inputs).  At the other end, fp16 keeps 11 bits only down to 2^-14; a state whose
+// entries all stay below 2^-12 (values of order 1e-5 and less) has lost accuracy in its
+// operands, so with check_small a CTA whose final state slice is nonzero but below 2^-12 sets
+// status bit 32.  The wide-range kernel takes values of any magnitude.
 //
 // Shared-memory layouts (tile bases 1024-byte aligned):
 //   [K; Q]   K-major, 128 B swizzle: [dk/64 blocks][128 rows][128 B]; rows 0..63 K, 64..127 Q
@@ -52,6 +55,8 @@ constexpr int kEpiThreads = 256;
 constexpr int kParts = 1;  // TMEM accumulators per phase (two in phase 1 measured 2 % slower)
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr int kStatusNonFinite = 16;
+constexpr int kStatusSmallState = 32;
+constexpr float kSmallState = 1.f / 4096.f;  // 2^-12: two bits above fp16's smallest normal value
 
 template <int DVT>
 struct CfgH {
@@ -175,7 +180,8 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                      const float* __restrict__ beta, const int32_t* __restrict__ cu,
                      const int32_t* __restrict__ chunk_off, const int32_t* __restrict__ order, const float* init,
                      __nv_bfloat16* __restrict__ out, float* fin, int* __restrict__ err, int B, int T, int Hk,
-                     int Hv, int DV, int nc_dense, long long nslots, int h_base, int c_begin, int c_end) {
+                     int Hv, int DV, int nc_dense, long long nslots, int h_base, int c_begin, int c_end,
+                     int check_small) {
   // The value tiles are inputs, ready before the preparation kernel finishes: for dense batches
   // the issue thread brings the first chunks' tiles into L2 before the wait below.
   if (cu == nullptr && threadIdx.x == 256) {
@@ -200,6 +206,7 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
   uint64_t* full = bars + 3;                                       // [0..kStages) stage loaded
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffBar + 48);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffBar + 52);
+  int* state_max = reinterpret_cast<int*>(sm + C::kOffBar + 56);  // bits of the largest |S| (non-negative floats order as ints)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 8;
@@ -247,6 +254,7 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
   if (tid == 0) {
     for (int i = 0; i < 3 + C::kStages; ++i) tc::mbar_init(&bars[i], 1);
     *abort_flag = 0;
+    *state_max = 0;
     tc::fence_mbar_init();
   }
   if (issuer && lane == 0) {
@@ -497,9 +505,18 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
   cp_async_wait<0>();
   if (!aborted && !issuer && d < DK) {
     bool finite = true;
+    float mx = 0.f;
 #pragma unroll
-    for (int i = 0; i < kCPT; ++i) finite = finite && fabsf(s[i]) <= 3.402823466e38f;
+    for (int i = 0; i < kCPT; ++i) {
+      finite = finite && fabsf(s[i]) <= 3.402823466e38f;
+      mx = fmaxf(mx, fabsf(s[i]));
+    }
     if (!finite) atomicOr(err, kStatusNonFinite);
+    if (check_small) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(__activemask(), mx, o));
+      if (lane == 0) atomicMax(state_max, __float_as_int(mx));
+    }
     if (fin != nullptr) {
       const size_t base = ((size_t)b * Hv + h) * DV + dv0 + kCPT * half;
 #pragma unroll
@@ -516,6 +533,10 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
   }
   tc::fence_before();
   __syncthreads();
+  if (check_small && !aborted && tid == 0) {
+    const float mx = __int_as_float(*state_max);
+    if (mx > 0.f && mx < kSmallState) atomicOr(err, kStatusSmallState);
+  }
   if (warp == 0) tc::tmem_dealloc(tmem, C::kTmemCols);
 }
 
@@ -524,7 +545,8 @@ cudaError_t launch_chain_f16_dvt(const void* v, const CUtensorMap& mw, const voi
                                  const float* beta, const int32_t* cu, const int32_t* chunk_off,
                                  const int32_t* order, const float* init, void* out, float* fin, int* err, int B,
                                  int T, int Hk, int Hv, int DV, int nc_dense, long long nslots, int h_base,
-                                 int h_count, int c_begin, int c_end, cuuint64_t tt, cudaStream_t st) {
+                                 int h_count, int c_begin, int c_end, int check_small, cuuint64_t tt,
+                                 cudaStream_t st) {
   using C = CfgH<DVT>;
   CUtensorMap mv;
   {
@@ -551,11 +573,13 @@ cudaError_t launch_chain_f16_dvt(const void* v, const CUtensorMap& mw, const voi
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, gdn_chain_f16_kernel<DK, DVT>, mv, mw, static_cast<const unsigned char*>(ws_kq), g,
                          beta, cu, chunk_off, order, init, static_cast<__nv_bfloat16*>(out), fin, err, B, T, Hk,
-                         Hv, DV, nc_dense, nslots, h_base, c_begin, c_end);
+                         Hv, DV, nc_dense, nslots, h_base, c_begin, c_end, check_small);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
+// check_small: report a final state below fp16's accurate range (status bit 32); off for the
+// two-level scan's inner runs, whose transition states may be legitimately tiny.
 // slice: state rows per CTA, 16, 32 or 64, or 0 for the library's choice.  The MMA issue and
 // the hand-offs of a chunk step do not depend on the width and its epilogues scale with it:
 // measured at 64 chunks, a 16-row step takes 0.91x a 32-row one and a 64-row step 1.41x.  So 64
@@ -567,7 +591,7 @@ cudaError_t launch_chain_f16(const void* v, const float* g, const float* beta, c
                              const int32_t* chunk_off, const int32_t* order, const void* ws, const void* ws_kq,
                              const float* init, void* out, float* fin, int* err, int B, int T, int Hk, int Hv,
                              int DV, int nc_dense, long long nslots, int h_base, int h_count, int c_begin,
-                             int c_end, int slice, cudaStream_t st) {
+                             int c_end, int slice, int check_small, cudaStream_t st) {
   const long long ttot = cu != nullptr ? (long long)T : (long long)B * T;
   const cuuint64_t tt = (cuuint64_t)(ttot > 0 ? ttot : 1);
   CUtensorMap mw;
@@ -594,14 +618,17 @@ cudaError_t launch_chain_f16(const void* v, const float* g, const float* beta, c
   switch (slice) {
     case 16:
       return launch_chain_f16_dvt<DK, 16>(v, mw, ws_kq, g, beta, cu, chunk_off, order, init, out, fin, err, B, T, Hk,
-                                          Hv, DV, nc_dense, nslots, h_base, h_count, c_begin, c_end, tt, st);
+                                          Hv, DV, nc_dense, nslots, h_base, h_count, c_begin, c_end, check_small,
+                                          tt, st);
     case 32:
       return launch_chain_f16_dvt<DK, 32>(v, mw, ws_kq, g, beta, cu, chunk_off, order, init, out, fin, err, B, T, Hk,
-                                          Hv, DV, nc_dense, nslots, h_base, h_count, c_begin, c_end, tt, st);
+                                          Hv, DV, nc_dense, nslots, h_base, h_count, c_begin, c_end, check_small,
+                                          tt, st);
     case 64:
       if (DV % 64 != 0) return cudaErrorInvalidValue;
       return launch_chain_f16_dvt<DK, 64>(v, mw, ws_kq, g, beta, cu, chunk_off, order, init, out, fin, err, B, T, Hk,
-                                          Hv, DV, nc_dense, nslots, h_base, h_count, c_begin, c_end, tt, st);
+                                          Hv, DV, nc_dense, nslots, h_base, h_count, c_begin, c_end, check_small,
+                                          tt, st);
     default:
       return cudaErrorInvalidValue;
   }
@@ -611,7 +638,7 @@ cudaError_t launch_chain_f16(const void* v, const float* g, const float* beta, c
   template cudaError_t launch_chain_f16<DK>(const void*, const float*, const float*, const int32_t*,           \
                                             const int32_t*, const int32_t*, const void*, const void*,          \
                                             const float*, void*, float*, int*, int, int, int, int, int, int,   \
-                                            long long, int, int, int, int, int, cudaStream_t);
+                                            long long, int, int, int, int, int, int, cudaStream_t);
 GDN_INST_CHAIN_F16(32)
 GDN_INST_CHAIN_F16(64)
 GDN_INST_CHAIN_F16(128)

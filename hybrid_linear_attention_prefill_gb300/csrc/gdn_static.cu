@@ -43,7 +43,7 @@ cudaError_t launch_wait_timeout_probe(int max_polls, int* status, cudaStream_t s
 template <int DK>
 cudaError_t launch_chain_f16(const void*, const float*, const float*, const int32_t*, const int32_t*,
                              const int32_t*, const void*, const void*, const float*, void*, float*, int*, int, int,
-                             int, int, int, int, long long, int, int, int, int, int, cudaStream_t);
+                             int, int, int, int, long long, int, int, int, int, int, int, cudaStream_t);
 }  // namespace gdn
 
 namespace {
@@ -139,9 +139,9 @@ extern "C" int gdn_prefill_static(const void* q, const void* k, const void* v, c
   }
   if (ev[1] != nullptr && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   switch (dk) {
-    case 32: e = gdn::launch_chain_f16<32>(v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_kq, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, Hv, 0, INT_MAX, 0, st); break;
-    case 64: e = gdn::launch_chain_f16<64>(v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_kq, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, Hv, 0, INT_MAX, 0, st); break;
-    default: e = gdn::launch_chain_f16<128>(v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_kq, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, Hv, 0, INT_MAX, 0, st); break;
+    case 32: e = gdn::launch_chain_f16<32>(v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_kq, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, Hv, 0, INT_MAX, 0, 1, st); break;
+    case 64: e = gdn::launch_chain_f16<64>(v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_kq, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, Hv, 0, INT_MAX, 0, 1, st); break;
+    default: e = gdn::launch_chain_f16<128>(v, g, beta, cu_seqlens, chunk_off, order, tiles, ws_kq, init_state, out, final_state, err, B, T, Hk, Hv, dv, nc_dense, nslots, 0, Hv, 0, INT_MAX, 0, 1, st); break;
   }
   if (e != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);
   if (ev[2] != nullptr && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return gdn::set_cuda_error(e, GDN_ERR_LAUNCH);

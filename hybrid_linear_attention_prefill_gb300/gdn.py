@@ -37,6 +37,7 @@ GDN_STATUS_LOAD_TIMEOUT = 2
 GDN_STATUS_PREP_LOAD_TIMEOUT = 4
 GDN_STATUS_BAD_CU_SEQLENS = 8
 GDN_STATUS_NONFINITE_STATE = 16
+GDN_STATUS_SMALL_STATE = 32
 
 
 def GDN_FLAG_SEGMENTS(n: int) -> int:

@@ -94,8 +94,11 @@ int gdn_last_cuda_error(void);
  * state-side operands rounded from the fp32 state (2^-11 relative).  The state
  * itself is carried in fp32.  Operands beyond fp16's range (about 65504: values of
  * that size, or a state that grows to it) make the state non-finite, which sets
- * GDN_STATUS_NONFINITE_STATE; gdn_prefill_ex with GDN_FLAG_WIDE_RANGE carries the
- * state-side operands as bf16 hi + lo pairs instead (fp32 range, 2^-16, slower).
+ * GDN_STATUS_NONFINITE_STATE.  Below it, fp16 keeps full precision only down to 2^-14:
+ * with values of order 1e-5 and less the operands lose accuracy, and a single-level
+ * call whose final state for some (sequence, head, row block) is nonzero but below
+ * 2^-12 sets GDN_STATUS_SMALL_STATE.  gdn_prefill_ex with GDN_FLAG_WIDE_RANGE carries
+ * the state-side operands as bf16 hi + lo pairs instead (fp32 range, 2^-16, slower).
  *
  * Memory.  The library keeps a per-device, grow-only workspace (allocated on the
  * first call that needs more; about 16 KB per 64-token chunk and value head, plus
@@ -282,6 +285,7 @@ int gdn_prefill_static(const void *q, const void *k, const void *v,
 #define GDN_STATUS_PREP_LOAD_TIMEOUT 4 /* the preparation kernel gave up waiting (tile load or Gram product) */
 #define GDN_STATUS_BAD_CU_SEQLENS 8    /* cu_seqlens was not 0 = cu[0] <= ... <= cu[B] = T (entries clamped) */
 #define GDN_STATUS_NONFINITE_STATE 16  /* a final state of the fp16 state carry was not finite (see gdn_prefill) */
+#define GDN_STATUS_SMALL_STATE 32      /* a final state of the fp16 state carry stayed below 2^-12 (see gdn_prefill) */
 
 /*
  * gdn_device_status -- synchronise the current device, return the status bits

@@ -143,6 +143,7 @@ def test_segment_flag_encoding():
     assert (gdn.GDN_FLAG_SLICE16, gdn.GDN_FLAG_SLICE32, gdn.GDN_FLAG_SLICE64) == (0x40000, 0x10000, 0x20000)
     assert "#define GDN_FLAG_WIDE_RANGE 0x80000u" in hdr and gdn.GDN_FLAG_WIDE_RANGE == 0x80000
     assert "#define GDN_STATUS_NONFINITE_STATE 16" in hdr and gdn.GDN_STATUS_NONFINITE_STATE == 16
+    assert "#define GDN_STATUS_SMALL_STATE 32" in hdr and gdn.GDN_STATUS_SMALL_STATE == 32
     assert "#define GDN_STATIC_SCRATCH_BYTES (128u << 20)" in hdr and gdn.GDN_STATIC_SCRATCH_BYTES == 128 << 20
 
 

@@ -7,7 +7,8 @@ also for the status word of the allocation-free entry point.  A malformed
 cu_seqlens is reported the same way, and a workspace allocation that fails (made
 to fail on the host) returns GDN_ERR_ALLOC before anything is launched.  Values
 beyond the fp16 operands' range make the default state carry's state non-finite,
-which its status bit reports; the wide-range state carry takes them.
+which its status bit reports; the wide-range state carry takes them.  So does a
+state too small for fp16's precision (values of order 1e-6), reported by its own bit.
 """
 
 import numpy as np
@@ -120,6 +121,30 @@ def test_values_beyond_fp16_range_are_reported_and_the_wide_range_carry_takes_th
     run_gpu(inp)
     rc, bits = gdn.gdn_device_status()
     assert rc == gdn.GDN_OK and bits == gdn.GDN_STATUS_NONFINITE_STATE
+    d = dev_inputs(inp)
+    out = torch.full((inp.total_tokens, inp.Hv, inp.dv), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fin = torch.full((inp.B, inp.Hv, inp.dv, inp.dk), float("nan"), device="cuda")
+    gdn.check(gdn.gdn_prefill_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], d["init"], out, fin,
+                                 inp.B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, gdn.GDN_FLAG_WIDE_RANGE))
+    torch.cuda.synchronize()
+    rc, bits = gdn.gdn_device_status()
+    assert rc == gdn.GDN_OK and bits == 0
+    o_ref, s_ref = oracle.prefill_inputs(inp)
+    o, s = out.float().cpu().numpy(), fin.cpu().numpy()
+    assert out_err(o, o_ref) <= OUT_TOL and state_err(s, s_ref) <= STATE_TOL
+
+
+def test_values_below_fp16_precision_are_reported_and_the_wide_range_carry_takes_them(gdn):
+    import oracle
+
+    from gpu_common import dev_inputs
+
+    inp = make_gdn_inputs(lengths=[130, 70], Hk=1, Hv=2, dk=128, dv=128, seed=85)
+    inp.v = f32_to_bf16_bits((inp.v64() * 1.0e-6).astype(np.float32))  # values of order 1e-6
+    gdn.gdn_device_status()
+    run_gpu(inp)
+    rc, bits = gdn.gdn_device_status()
+    assert rc == gdn.GDN_OK and bits == gdn.GDN_STATUS_SMALL_STATE
     d = dev_inputs(inp)
     out = torch.full((inp.total_tokens, inp.Hv, inp.dv), float("nan"), dtype=torch.bfloat16, device="cuda")
     fin = torch.full((inp.B, inp.Hv, inp.dv, inp.dk), float("nan"), device="cuda")

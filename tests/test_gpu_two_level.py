@@ -82,6 +82,14 @@ def test_no_decay_strong_writes(gdn):
     _check_oracle(o, s, inp)
 
 
+@pytest.mark.parametrize("P", [3, 4])
+def test_wide_range_state_carry(gdn, P):
+    """The two-level scan on the bf16 hi / lo state carry (its transition runs included)."""
+    inp = make_gdn_inputs(B=2, T=700, Hk=2, Hv=4, dk=128, dv=128, seed=98 + P, g_scale=0.05, init_std=0.1)
+    o, s = _run(gdn, inp, _two(gdn, P) | gdn.GDN_FLAG_WIDE_RANGE)
+    _check_oracle(o, s, inp)
+
+
 def test_zero_init_and_no_final_state(gdn):
     inp = make_gdn_inputs(B=1, T=640, Hk=1, Hv=1, dk=128, dv=128, seed=98, g_scale=0.05)
     o, _ = _run(gdn, inp, _two(gdn, 5), want_final=False)
