@@ -3,7 +3,7 @@
 Each case draws, from its own seed: dense or packed (with empty and single-token sequences among
 the lengths), the key/value head counts and their ratio, dk and dv, the decay scale, an initial
 state or none, and the entry flags (slice width 16 / 32 / 64 / the library's choice, in-kernel q/k
-normalisation).  Sizes stay small enough for the oracle to finish in about a second each, and
+normalisation, the wide-range operand format).  Sizes stay small enough for the oracle to finish in about a second each, and
 large enough to span several chunks and a ragged tail."""
 
 import numpy as np
@@ -49,6 +49,8 @@ def _draw(seed, gdn):
                          ([gdn.GDN_FLAG_SLICE64] if dv % 64 == 0 else [])))
     if not normalize:
         flags |= gdn.GDN_FLAG_L2NORM_QK
+    if r.random() < 0.25:  # the wide-range (bf16 hi / lo) state carry
+        flags |= gdn.GDN_FLAG_WIDE_RANGE
     inp = make_gdn_inputs(Hk=Hk, Hv=Hv, dk=dk, dv=dv, seed=2000 + seed, g_scale=g_scale, init_std=init_std,
                           normalize_qk=normalize, **kw)
     return inp, flags
