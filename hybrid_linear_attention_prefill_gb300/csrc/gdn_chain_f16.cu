@@ -191,11 +191,18 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     for (int cc = c_begin; cc < c_begin + CfgH<DVT>::kStages && cc * kChunk < T; ++cc)
       tc::tma_prefetch_l2_3d(&tm_v, d0, hh, (int)((long long)bb * T + (long long)cc * kChunk));
   }
+  using C = CfgH<DVT>;
+  if (threadIdx.x == 0) {  // the barriers need nothing from the kernel before
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t r = smem_u32(smem_raw);
+    uint64_t* bb = reinterpret_cast<uint64_t*>(smem_raw + (((r + 1023u) & ~1023u) - r) + C::kOffBar);
+    for (int i = 0; i < 3 + C::kStages; ++i) tc::mbar_init(&bb[i], 1);
+    tc::fence_mbar_init();
+  }
   // Launched as a programmatic dependent of the kernel before it in the stream (the preparation
   // kernel): the CTA starts while that kernel's last CTAs run and waits here until it has
   // completed and its writes are visible (otherwise this returns at once).
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  using C = CfgH<DVT>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t pad = ((raw_s + 1023u) & ~1023u) - raw_s;
@@ -252,7 +259,6 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 3 + C::kStages; ++i) tc::mbar_init(&bars[i], 1);
     *abort_flag = 0;
     *state_max = 0;
     tc::fence_mbar_init();
