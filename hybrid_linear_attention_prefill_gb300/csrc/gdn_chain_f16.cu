@@ -336,9 +336,20 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     const uint32_t par = (uint32_t)(ci & 1);
     unsigned char* st = sm + stg * C::kStage;
     cp_async_wait<0>();
-    if (!tc::mbar_wait(&full[stg], (uint32_t)((ci / C::kStages) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
+    // The stage's tiles: the thread that issued their copies waits for them, then the barrier
+    // below publishes them to every thread (it makes the accesses that thread requested and saw
+    // complete visible to all the CTA's threads).  The epilogue warps read the value slice after
+    // that barrier without waiting themselves: 256 waits on a completed phase cost the chunk step
+    // ~4 % at the headline size.
+    if (issuer && lane == 0 && !tc::mbar_wait(&full[stg], (uint32_t)((ci / C::kStages) & 1), kMaxPolls)) {
+      *abort_flag = 1;
+      atomicOr(err, 2);
+    }
     __syncthreads();
-    if (*abort_flag) { aborted = true; break; }
+    // Every thread reads the abort flag right after each barrier, so all of them leave the loop
+    // at the same barrier; the issuing thread acts on it after issuing that phase's MMAs (which
+    // an abort makes harmless), so the read is off its path to the tensor core.
+    const int ab_top = *abort_flag;
 
     if (issuer) {
       // Descriptors: this stage's bases plus each MMA's offset, added to the start-address field
@@ -361,8 +372,9 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         if (c + kAhead < c1) load_tiles(c + kAhead, (ci + kAhead) % C::kStages);
       }
       __syncwarp();
+      if (ab_top) { aborted = true; break; }
       __syncthreads();  // R written
-      if (*abort_flag) { aborted = true; break; }
+      const int ab_r = *abort_flag;
       // ---- phase 2: [U; Z] = [Tm; PT] R ---------------------------------------------
       if (lane == 0) {
         tc::fence_after();
@@ -372,8 +384,9 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         tc::commit(&bars[1]);
       }
       __syncwarp();
+      if (ab_r) { aborted = true; break; }
       __syncthreads();  // dU written
-      if (*abort_flag) { aborted = true; break; }
+      const int ab_d = *abort_flag;
       // ---- phase 3: dS^T = K^T dU ---------------------------------------------------
       if (lane == 0) {
         tc::fence_after();
@@ -383,10 +396,12 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         tc::commit(&bars[2]);
       }
       __syncwarp();
+      if (ab_d) { aborted = true; break; }
       continue;
     }
 
     // ================= epilogue warps =================
+    if (ab_top) { aborted = true; break; }
     if (c + 1 < c1) load_scalars(c + 1, (ci + 1) % C::kStages);
     cp_async_commit();
 

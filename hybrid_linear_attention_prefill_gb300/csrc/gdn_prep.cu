@@ -284,9 +284,13 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       load_gb(cur, 0, 0);
       if (tid == 0 && item != ahead) load_tiles(item, cur);
     }
-    if (!tc::mbar_wait(&bar[0], ph, 1u << 24)) atomicOr(err, 4);
-    // rows t >= n belong to the next sequence (or are past the end): clear them
+    // Thread 0 issued the tile copies and waits for them; the barriers below publish the tiles
+    // to the other threads (a barrier makes the accesses a thread requested and saw complete
+    // visible to all), so 255 more waits on the same phase are not needed.
+    if (tid == 0 && !tc::mbar_wait(&bar[0], ph, 1u << 24)) atomicOr(err, 4);
+    // rows t >= n belong to the next sequence (or are past the end): clear them once the copy is in
     if (n < kChunk) {
+      __syncthreads();
       for (int e = tid; e < kKBlocks * 2 * (kChunk - n) * 8; e += kPrepThreads) {
         const int piece = e & 7, rr = e >> 3;
         const int r = n + rr % (kChunk - n), which = (rr / (kChunk - n)) & 1, db = rr / (2 * (kChunk - n));
@@ -320,9 +324,10 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     // without normalisation the image needs no norms: written while the product runs (the
     // tensor core only reads the tile)
     if (F16 && !norm_qk) write_kq_image(false);
-    if (!tc::mbar_wait(&bar[1], ph, 1u << 24)) atomicOr(err, 4);
-    tc::fence_after();
+    if (tid == 0 && !tc::mbar_wait(&bar[1], ph, 1u << 24)) atomicOr(err, 4);  // its own MMAs' commit
+    tc::fence_before();
     __syncthreads();  // Grams done (they stay in TMEM) and norms visible; the tiles are dead after the image
+    tc::fence_after();
 
     if (F16 && norm_qk) write_kq_image(true);  // scaled by the norms just summed
 
