@@ -338,9 +338,15 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     unsigned char* st = sm + stg * C::kStage;
     const uint32_t st_s = sb + stg * C::kStage;
     cp_async_wait<0>();
-    if (!tc::mbar_wait(&full[stg], (uint32_t)((ci / C::kStages) & 1), kMaxPolls)) { *abort_flag = 1; atomicOr(err, 2); }
+    // The thread that issued the stage's copies waits for them; the barrier publishes them to
+    // every thread.  All threads read the abort flag right after each barrier (so they leave the
+    // loop at the same one); the issuing thread acts on it after issuing that phase's MMAs.
+    if (issuer && lane == 0 && !tc::mbar_wait(&full[stg], (uint32_t)((ci / C::kStages) & 1), kMaxPolls)) {
+      *abort_flag = 1;
+      atomicOr(err, 2);
+    }
     __syncthreads();
-    if (*abort_flag) { aborted = true; break; }
+    const int ab_top = *abort_flag;
 
     if (issuer) {
       // ---- phase 1: [X; Y] = [K; Q] [S_hi | S_lo]^T --------------------------------
@@ -358,8 +364,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (c + kAhead < c1) load_tiles(c + kAhead, (ci + kAhead) % C::kStages);
       }
       __syncwarp();
+      if (ab_top) { aborted = true; break; }
       __syncthreads();  // R written
-      if (*abort_flag) { aborted = true; break; }
+      const int ab_r = *abort_flag;
       // ---- phase 2: [U; Z] = [Tm; PT] [R_hi | R_lo] --------------------------------
       if (lane == 0) {
         tc::fence_after();
@@ -372,8 +379,9 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         tc::commit(&bars[1]);
       }
       __syncwarp();
+      if (ab_r) { aborted = true; break; }
       __syncthreads();  // dU written
-      if (*abort_flag) { aborted = true; break; }
+      const int ab_d = *abort_flag;
       // ---- phase 3: dS^T = K^T [dU_hi | dU_lo] -------------------------------------
       if (lane == 0) {
         tc::fence_after();
@@ -386,10 +394,12 @@ gdn_chain_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         tc::commit(&bars[2]);
       }
       __syncwarp();
+      if (ab_d) { aborted = true; break; }
       continue;
     }
 
     // ================= epilogue warps =================
+    if (ab_top) { aborted = true; break; }
     if (c + 1 < c1) load_scalars(c + 1, (ci + 1) % C::kStages);
     cp_async_commit();
 
