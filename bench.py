@@ -81,8 +81,9 @@ def read_peaks():
                 source="measured" if hbm else "fallback")
 
 
-def traffic_record(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+def traffic_record(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this workload and the
+    kernel source is unchanged since."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -91,7 +92,7 @@ def traffic_record(kernel):
             rec = json.load(f).get(kernel)
     except (OSError, ValueError):
         return None
-    if not rec:
+    if not rec or rec.get("workload") != workload:
         return None
     src = os.path.join(ROOT, "hybrid_linear_attention_prefill_gb300", "csrc", rec["source"])
     try:
@@ -367,7 +368,7 @@ def run_gpu_arm(args):
     achieved = dom_bytes / (kernels[dom] * 1e-3) / 1e9
     segs = gdn.gdn_scan_segments(B, inp.T, inp.Hk, inp.Hv, inp.dk, inp.dv, d["cu"] is not None,
                                  0 if flags is None else flags)
-    trec = traffic_record(dom) if segs == 1 else None  # the ncu record is of the single-level launch
+    trec = traffic_record(dom, args.workload) if segs == 1 else None  # the record: one single-level launch
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
                 "traffic": None if trec is None else trec["dram_bytes_per_launch"],

@@ -69,3 +69,27 @@ def test_reference_arm_prints_only_on_rank_zero(capsys, monkeypatch):
 
     bench.run_reference_arm(A())
     assert capsys.readouterr().out == ""
+
+
+def test_traffic_record_only_for_its_workload_and_source(tmp_path, monkeypatch):
+    """The committed ncu traffic figure is reported only for the workload it was captured on and
+    only while the kernel source still hashes to the recorded value."""
+    import hashlib
+    import json
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    src_dir = tmp_path / "hybrid_linear_attention_prefill_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (src_dir / "k.cu").write_bytes(b"kernel v1")
+    rec = {"source": "k.cu", "source_sha256_16": hashlib.sha256(b"kernel v1").hexdigest()[:16],
+           "workload": "wl_a", "dram_bytes_per_launch": 123}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"gdn_chain_kernel": rec}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("gdn_chain_kernel", "wl_a")["dram_bytes_per_launch"] == 123
+    assert bench.traffic_record("gdn_chain_kernel", "wl_b") is None       # another workload
+    assert bench.traffic_record("gdn_prep_kernel", "wl_a") is None        # no record
+    (src_dir / "k.cu").write_bytes(b"kernel v2")
+    assert bench.traffic_record("gdn_chain_kernel", "wl_a") is None       # source changed since
