@@ -23,9 +23,9 @@
 // value heads that share the key head, so the Grams K K^T and Q K^T are computed
 // once per key head (one tcgen05 product in TMEM).  The inverse is blocked: the
 // four 16 x 16 diagonal blocks by forward substitution in fp32, then the
-// 16 -> 32 -> 64 merges T21 = -T22 A21 T11 as tensor-core products of the fp32
-// blocks rounded to fp16 (fp32 accumulate).  Only non-positive exponents are ever
-// taken (gamma_t - gamma_i, i <= t), so nothing overflows however strong the decay.
+// 16 -> 32 -> 64 merges T21 = -T22 A21 T11 as tensor-core products of fp16 blocks
+// (each rounded once, when it is formed; fp32 accumulate).  Only non-positive exponents
+// are ever taken (gamma_t - gamma_i, i <= t), so nothing overflows however strong the decay.
 #include <atomic>
 #include <cuda_fp16.h>
 #include "gdn_tc.cuh"
@@ -37,39 +37,14 @@ namespace {
 
 constexpr int kPrepThreads = 256;
 constexpr int kPrepCtasPerSm = 4;  // resident CTAs per SM: registers by the launch bounds, shared memory below
-constexpr int LDF = 68;  // fp32 row stride of 64-wide matrices
-constexpr int LDB = 72;  // bf16 row stride of 64-wide matrices
-constexpr int LDW = 36;  // fp32 row stride of the 32-wide merge buffer
-constexpr int LDE = 20;  // fp32 row stride of the 16-wide decay tables
+constexpr int LDB = 72;   // 16-bit row stride of 64-wide matrices (144 B: ldmatrix rows on distinct banks)
+constexpr int LDWH = 40;  // 16-bit row stride of the 32-wide merge buffer (80 B, likewise)
+constexpr int LDD = 20;   // fp32 row stride of A's 16 x 16 diagonal blocks
+constexpr int LDE = 20;   // fp32 row stride of the 16-wide decay tables
 
 __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// acc (16 x 8 tile) += X[r0:r0+16, k0:k0+16] * Y[ky:ky+16, n0:n0+8] for fp32 X, Y in shared
-// memory, as one m16n8k16 product of their fp16 roundings (fp32 accumulate).  It serves the
-// 16 -> 32 -> 64 merges of the blocked inverse: with unit-norm keys and beta <= 1 the blocks of
-// (I + A)^-1 stay of order one, well inside fp16's range, and fp16's 2^-11 rounding is far below
-// the bf16 rounding (2^-8) the finished Tm gets.  A float64 model of the whole path gives the
-// same final-state error as with 2^-16-accurate hi/lo bf16 merges (1.055e-3 against 1.053e-3 on
-// a no-decay, beta = 0.999 stress case).
-__device__ __forceinline__ void mma_f16x1(float (&acc)[4], const float* X, int ldx, int r0, int k0,
-                                          const float* Y, int ldy, int ky, int n0, int lane) {
-  const int g8 = lane >> 2, tg = lane & 3;
-  const float2 x0 = *reinterpret_cast<const float2*>(X + (r0 + g8) * ldx + k0 + 2 * tg);
-  const float2 x1 = *reinterpret_cast<const float2*>(X + (r0 + g8 + 8) * ldx + k0 + 2 * tg);
-  const float2 x2 = *reinterpret_cast<const float2*>(X + (r0 + g8) * ldx + k0 + 8 + 2 * tg);
-  const float2 x3 = *reinterpret_cast<const float2*>(X + (r0 + g8 + 8) * ldx + k0 + 8 + 2 * tg);
-  const uint32_t a0 = pack_f16(x0.x, x0.y), a1 = pack_f16(x1.x, x1.y), a2 = pack_f16(x2.x, x2.y),
-                 a3 = pack_f16(x3.x, x3.y);
-  const uint32_t b0 = pack_f16(Y[(ky + 2 * tg) * ldy + n0 + g8], Y[(ky + 2 * tg + 1) * ldy + n0 + g8]);
-  const uint32_t b1 = pack_f16(Y[(ky + 2 * tg + 8) * ldy + n0 + g8], Y[(ky + 2 * tg + 9) * ldy + n0 + g8]);
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Two values as the 16-bit format of the stored tiles: fp16 or bf16.
@@ -93,31 +68,66 @@ __device__ __forceinline__ void mma16(float (&d)[4], const uint32_t (&a)[4], uin
   }
 }
 
-// Store a 16 x 8 accumulator tile (times `sgn`) at D[r0.., n0..].
-__device__ __forceinline__ void store_tile(float* D, int ldd, int r0, int n0, const float (&acc)[4], float sgn,
-                                           int lane) {
+// ldmatrix for the merges' fp16 operands (the memory clobber keeps them after the stores they read)
+__device__ __forceinline__ void ldsm_a(uint32_t (&r)[4], const uint16_t* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p))
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_b_t(uint32_t (&r)[4], const uint16_t* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p))
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_b8_t(uint32_t (&r)[2], const uint16_t* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(p))
+               : "memory");
+}
+
+// The m16n8k16 A fragment of the 16 x 16 fp16 block at X[r0.., k0..] (row stride ld), and the
+// B fragment of the 16 x 8 block at Y[k0.., n0..] (row-major, k rows).
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const uint16_t* X, int ld, int r0, int k0, int lane) {
+  const int m = lane >> 3;
+  ldsm_a(a, X + (r0 + 8 * (m & 1) + (lane & 7)) * ld + k0 + 8 * (m >> 1));
+}
+__device__ __forceinline__ void frag_b8(uint32_t (&b)[2], const uint16_t* Y, int ld, int k0, int n0, int lane) {
+  ldsm_b8_t(b, Y + (k0 + (lane & 15)) * ld + n0);
+}
+
+// Store a 16 x 8 accumulator tile (times `sgn`), rounded to fp16, at D[r0.., n0..].
+__device__ __forceinline__ void store_tile_h(uint16_t* D, int ldd, int r0, int n0, const float (&acc)[4], float sgn,
+                                             int lane) {
   const int g8 = lane >> 2, tg = lane & 3;
-  *reinterpret_cast<float2*>(D + (r0 + g8) * ldd + n0 + 2 * tg) = make_float2(sgn * acc[0], sgn * acc[1]);
-  *reinterpret_cast<float2*>(D + (r0 + g8 + 8) * ldd + n0 + 2 * tg) = make_float2(sgn * acc[2], sgn * acc[3]);
+  *reinterpret_cast<uint32_t*>(D + (r0 + g8) * ldd + n0 + 2 * tg) = pack_f16(sgn * acc[0], sgn * acc[1]);
+  *reinterpret_cast<uint32_t*>(D + (r0 + g8 + 8) * ldd + n0 + 2 * tg) = pack_f16(sgn * acc[2], sgn * acc[3]);
 }
 
 }  // namespace
 
 template <int DK>
 struct PrepSmem {
-  // [union: K,Q tiles (TMA, 128 B swizzle) | A,Tm fp32] [P 16-bit] [Tm 16-bit | decay tables |
-  // merge buffer] [inverse norms] [column factors] [g, beta] [mbarriers]
-  // (the Grams stay in TMEM; the CTA fits four times on an SM).  Within a value head the decay
-  // tables live until A and P are built, the merge buffer through the 16 -> 32 -> 64 merges and
-  // the 16-bit Tm from then on, so the three share one region.
+  // [union: K,Q tiles (TMA, 128 B swizzle) | the inverse's working set] [P 16-bit]
+  // [Tm 16-bit | decay tables] [inverse norms] [column factors] [g, beta] [mbarriers]
+  // (the Grams stay in TMEM; the CTA fits four times on an SM).  The working set of the inverse
+  // -- A's blocks below the diagonal and Tm in fp16 (the merges' operands, each rounded once),
+  // A's diagonal blocks in fp32 (the forward substitution), the fp16 merge buffer -- lives over
+  // the key and query tiles, which are dead once the Grams and the image are done.  Within a
+  // value head the decay tables live until A and P are built and the 16-bit Tm from then on, so
+  // the two share one region.
   static constexpr int kKQBytes = 32768;
-  static constexpr int kATBytes = 2 * kChunk * LDF * 4;
-  static constexpr int kUnion = kKQBytes > kATBytes ? kKQBytes : kATBytes;
+  static constexpr int offAh = 0;                          // [64][LDB] fp16
+  static constexpr int offTh = offAh + kChunk * LDB * 2;   // [64][LDB] fp16
+  static constexpr int offAd = offTh + kChunk * LDB * 2;   // [4][16][LDD] fp32
+  static constexpr int offWh = offAd + 4 * 16 * LDD * 4;   // [32][LDWH] fp16
+  static constexpr int kMergeBytes = offWh + 32 * LDWH * 2;
+  static constexpr int kUnion = kKQBytes > kMergeBytes ? kKQBytes : kMergeBytes;
   static constexpr int offP = kUnion;
   static constexpr int offTb = offP + kChunk * LDB * 2;
-  static constexpr int offW = offTb;                   // the merge buffer, over the bf16 Tm
   static constexpr int offRN = offTb + kChunk * LDB * 2;  // inverse norms of k rows, then q rows
-  static_assert(32 * LDW * 4 <= kChunk * LDB * 2, "the merge buffer fits over the 16-bit Tm");
   static_assert(4 * 16 * LDE * 4 + kChunk * 4 * 4 <= kChunk * LDB * 2, "the decay tables fit over the 16-bit Tm");
   static constexpr int offCF = offRN + 2 * kChunk * 4;  // column factors [64]
   static constexpr int offGB = offCF + kChunk * 4;       // [2 buffers][g 64 | beta 64] fp32
@@ -140,11 +150,13 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const uint32_t raw_s = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   unsigned char* KQ = smem;                    // [2][128][128 B], swizzled
-  float* As = reinterpret_cast<float*>(smem);  // aliases K/Q after the Grams
-  float* Tms = As + kChunk * LDF;
+  // the inverse's working set, over K / Q after the Grams
+  uint16_t* Ah = reinterpret_cast<uint16_t*>(smem + L::offAh);  // A below its diagonal blocks, fp16
+  uint16_t* Th = reinterpret_cast<uint16_t*>(smem + L::offTh);  // Tm, fp16
+  float* Ad = reinterpret_cast<float*>(smem + L::offAd);         // A's diagonal blocks, fp32
+  uint16_t* Wh = reinterpret_cast<uint16_t*>(smem + L::offWh);  // merge buffer, fp16
   uint16_t* Ps = reinterpret_cast<uint16_t*>(smem + L::offP);
   uint16_t* Tmb = reinterpret_cast<uint16_t*>(smem + L::offTb);
-  float* Wt = reinterpret_cast<float*>(smem + L::offW);  // [32][LDW]
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::offBar);  // [0] tiles loaded, [1] Grams done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offBar + 16);
   float* gbuf = reinterpret_cast<float*>(smem + L::offGB);
@@ -376,7 +388,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
       __syncthreads();
 
-      // ---- A (fp32) and P (16-bit) straight from the Grams in TMEM ---------------------
+      // ---- A and P (16-bit) straight from the Grams in TMEM ------------------------------
       // Warp w reads TMEM lanes 32 (w % 4) .. + 31 -- rows 0..63 of the Gram are K K^T (A),
       // rows 64..127 Q K^T (P) -- and columns 32 (w / 4) .. + 31, 16 at a time.  A row's
       // entries in a 16-column block are the Gram's times one factor per row and one per
@@ -391,10 +403,10 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         for (int sb = 0; sb < 2; ++sb) {
           const int cb = 32 * hf + 16 * sb;
           float o[16];
+          const bool own = t >= cb && t < cb + 16, below = t >= cb + 16;
           if (cb <= 32 * (q4 & 1) + 31) {  // warp-uniform: some row of the warp reaches column cb
             float v[16];
             tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + cb, v);
-            const bool own = t >= cb && t < cb + 16, below = t >= cb + 16;
             const float* fp = own ? Es + t * LDE : cfs + cb;  // column factors of this row
             const float s = own ? sc : below ? sc * rfs[4 * t + (cb >> 4)] : 0.f;
 #pragma unroll
@@ -415,10 +427,19 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             for (int u = 0; u < 16; ++u) o[u] = 0.f;
           }
           if (isA) {
-            float* arow = As + t * LDF + cb;
+            if (own) {  // the diagonal block in fp32, for the forward substitution
+              float* arow = Ad + (cb >> 4) * 16 * LDD + (t - cb) * LDD;
 #pragma unroll
-            for (int p = 0; p < 4; ++p)
-              *reinterpret_cast<float4*>(arow + 4 * p) = make_float4(o[4 * p], o[4 * p + 1], o[4 * p + 2], o[4 * p + 3]);
+              for (int p = 0; p < 4; ++p)
+                *reinterpret_cast<float4*>(arow + 4 * p) = make_float4(o[4 * p], o[4 * p + 1], o[4 * p + 2], o[4 * p + 3]);
+            } else if (below) {  // fp16, the merges' operands (the blocks above are never read)
+              uint16_t* arow = Ah + t * LDB + cb;
+#pragma unroll
+              for (int p = 0; p < 2; ++p)
+                *reinterpret_cast<uint4*>(arow + 8 * p) =
+                    make_uint4(pack_f16(o[8 * p], o[8 * p + 1]), pack_f16(o[8 * p + 2], o[8 * p + 3]),
+                               pack_f16(o[8 * p + 4], o[8 * p + 5]), pack_f16(o[8 * p + 6], o[8 * p + 7]));
+            }
           } else {
             uint16_t* prow = Ps + t * LDB + cb;
 #pragma unroll
@@ -431,9 +452,9 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
       tc::fence_before();  // the TMEM reads are ordered before the next item's Gram product
       if (gi == 0) {  // the blocks of Tm above the diagonal stay zero for every value head
-        for (int e = tid; e < kChunk * 16; e += kPrepThreads) {
-          const int t = e >> 4, c4 = (e & 15) * 4;
-          if ((c4 >> 4) > (t >> 4)) *reinterpret_cast<float4*>(Tms + t * LDF + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
+          const int t = e >> 3, c8 = (e & 7) * 8;
+          if ((c8 >> 4) > (t >> 4)) *reinterpret_cast<uint4*>(Th + t * LDB + c8) = make_uint4(0, 0, 0, 0);
         }
       }
       __syncthreads();
@@ -444,7 +465,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       // the dependent chain is one FMA per row).
       if (tid < 64) {
         const int blk = tid >> 4, j = tid & 15;
-        const float* Ab = As + 16 * blk * LDF + 16 * blk;
+        const float* Ab = Ad + blk * 16 * LDD;
         float x[16], accv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) { x[i] = (i == j) ? 1.f : 0.f; accv[i] = 0.f; }
@@ -452,62 +473,81 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         for (int i = 0; i < 15; ++i) {
           if (i > j) x[i] = -accv[i];
 #pragma unroll
-          for (int t = i + 1; t < 16; ++t) accv[t] = fmaf(Ab[t * LDF + i], x[i], accv[t]);
+          for (int t = i + 1; t < 16; ++t) accv[t] = fmaf(Ab[t * LDD + i], x[i], accv[t]);
         }
         if (15 > j) x[15] = -accv[15];
-        float* Tb = Tms + 16 * blk * LDF + 16 * blk;
+        uint16_t* Tb = Th + 16 * blk * LDB + 16 * blk;  // fp16: the merges' operand and the 16-bit Tm
 #pragma unroll
-        for (int t = 0; t < 16; ++t) Tb[t * LDF + j] = x[t];
+        for (int t = 0; t < 16; ++t) Tb[t * LDB + j] = __half_as_ushort(__float2half_rn(x[t]));
       }
       __syncthreads();
 
       // ---- merge 16 -> 32: T[o+16.., o..] = -T22 (A21 T11), o = 0 and 32 -------
       // Warp w < 4 forms the 8-column tile nt = w % 2 of block o = 32 (w / 2): its column
-      // tile of W = A21 T11 is all that its tile of T21 = -T22 W needs.
+      // tile of W = A21 T11 is all that its tile of T21 = -T22 W needs.  Operands by ldmatrix
+      // from the fp16 blocks; the products accumulate in fp32 and are rounded to fp16 once.
       if (warp < 4) {
         const int o = 32 * (warp >> 1), nt = warp & 1;
-        float* W = Wt + 16 * (warp >> 1) * LDW;  // this block's 16 x 16 part of the buffer
+        uint16_t* W = Wh + 16 * (warp >> 1) * LDWH;  // this block's 16 x 16 part of the buffer
+        uint32_t a[4], b[2];
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f16x1(acc, As, LDF, o + 16, o, Tms, LDF, o, o + 8 * nt, lane);
-        store_tile(W, LDW, 0, 8 * nt, acc, 1.f, lane);
+        frag_a(a, Ah, LDB, o + 16, o, lane);
+        frag_b8(b, Th, LDB, o, o + 8 * nt, lane);
+        mma16<true>(acc, a, b[0], b[1]);
+        store_tile_h(W, LDWH, 0, 8 * nt, acc, 1.f, lane);
         __syncwarp();
         float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f16x1(acc2, Tms, LDF, o + 16, o + 16, W, LDW, 0, 8 * nt, lane);
-        store_tile(Tms, LDF, o + 16, o + 8 * nt, acc2, -1.f, lane);
+        frag_a(a, Th, LDB, o + 16, o + 16, lane);
+        frag_b8(b, W, LDWH, 0, 8 * nt, lane);
+        mma16<true>(acc2, a, b[0], b[1]);
+        store_tile_h(Th, LDB, o + 16, o + 8 * nt, acc2, -1.f, lane);
       }
       __syncthreads();
 
       // ---- merge 32 -> 64: T[32.., 0..32] = -T[32..,32..] (A[32..,0..32] T[0..32,0..32]) ----
       {
         const int mt = warp >> 2, nt = warp & 3;
+        uint32_t a[4], b[2];
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) mma_f16x1(acc, As, LDF, 32 + 16 * mt, 16 * kk, Tms, LDF, 16 * kk, 8 * nt, lane);
-        store_tile(Wt, LDW, 16 * mt, 8 * nt, acc, 1.f, lane);
+        for (int kk = 0; kk < 2; ++kk) {
+          frag_a(a, Ah, LDB, 32 + 16 * mt, 16 * kk, lane);
+          frag_b8(b, Th, LDB, 16 * kk, 8 * nt, lane);
+          mma16<true>(acc, a, b[0], b[1]);
+        }
+        store_tile_h(Wh, LDWH, 16 * mt, 8 * nt, acc, 1.f, lane);
         __syncthreads();
         float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-          mma_f16x1(acc2, Tms, LDF, 32 + 16 * mt, 32 + 16 * kk, Wt, LDW, 16 * kk, 8 * nt, lane);
-        store_tile(Tms, LDF, 32 + 16 * mt, 8 * nt, acc2, -1.f, lane);
+        for (int kk = 0; kk < 2; ++kk) {
+          frag_a(a, Th, LDB, 32 + 16 * mt, 32 + 16 * kk, lane);
+          frag_b8(b, Wh, LDWH, 16 * kk, 8 * nt, lane);
+          mma16<true>(acc2, a, b[0], b[1]);
+        }
+        store_tile_h(Th, LDB, 32 + 16 * mt, 8 * nt, acc2, -1.f, lane);
       }
       __syncthreads();
 
       // ---- 16-bit Tm: to shared (for PT) and to the workspace ------------------
+      // fp16 as it stands; the wide-range path's bf16 from those fp16 values
       uint16_t* wsT = ws + ((size_t)slot * Hv + h) * (2 * kWsTileElems);
       uint16_t* wsPT = wsT + kWsTileElems;
       for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
         const int r = e >> 3, p = e & 7;
-        const float* src = Tms + r * LDF + 8 * p;
-        uint4 v;
-        v.x = pack16<F16>(src[0], src[1]);
-        v.y = pack16<F16>(src[2], src[3]);
-        v.z = pack16<F16>(src[4], src[5]);
-        v.w = pack16<F16>(src[6], src[7]);
+        uint4 v = *reinterpret_cast<const uint4*>(Th + r * LDB + 8 * p);
+        if constexpr (!F16) {
+          uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
+            w4[q] = pack16<false>(f.x, f.y);
+          }
+          v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
         *reinterpret_cast<uint4*>(Tmb + r * LDB + 8 * p) = v;
         *reinterpret_cast<uint4*>(wsT + r * kChunk + 8 * p) = v;
       }
-      if (gi == G - 1) tc::fence_proxy_async();  // fp32 A and Tm are dead: the next tiles may land over them
+      if (gi == G - 1) tc::fence_proxy_async();  // the inverse's working set is dead: the next tiles may land over it
       __syncthreads();
       if (gi == G - 1 && tid == 0) {  // the CTA's next item's tile copy overlaps PT and the stores
         for (int nx = item + (int)gridDim.x; nx < n_items; nx += gridDim.x) {
