@@ -40,6 +40,9 @@ constexpr int kPrepCtasPerSm = 4;  // resident CTAs per SM: registers by the lau
 constexpr int LDB = 72;   // 16-bit row stride of 64-wide matrices (144 B: ldmatrix rows on distinct banks)
 constexpr int LDWH = 40;  // 16-bit row stride of the 32-wide merge buffer (80 B, likewise)
 constexpr int LDD = 20;   // fp32 row stride of A's 16 x 16 diagonal blocks
+// ... and the stride between those blocks: 16 banks apart, so the substitution's two blocks per
+// warp (one per half-warp, every lane of a half reading the same entry) take one wavefront
+constexpr int kDiagStride = 16 * LDD + 16;
 constexpr int LDE = 20;   // fp32 row stride of the 16-wide decay tables
 
 __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
@@ -121,8 +124,8 @@ struct PrepSmem {
   static constexpr int kKQBytes = 32768;
   static constexpr int offAh = 0;                          // [64][LDB] fp16
   static constexpr int offTh = offAh + kChunk * LDB * 2;   // [64][LDB] fp16
-  static constexpr int offAd = offTh + kChunk * LDB * 2;   // [4][16][LDD] fp32
-  static constexpr int offWh = offAd + 4 * 16 * LDD * 4;   // [32][LDWH] fp16
+  static constexpr int offAd = offTh + kChunk * LDB * 2;   // [4][16][LDD] fp32, blocks kDiagStride apart
+  static constexpr int offWh = offAd + 4 * kDiagStride * 4;  // [32][LDWH] fp16
   static constexpr int kMergeBytes = offWh + 32 * LDWH * 2;
   static constexpr int kUnion = kKQBytes > kMergeBytes ? kKQBytes : kMergeBytes;
   static constexpr int offP = kUnion;
@@ -165,9 +168,9 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   float* cfs = reinterpret_cast<float*>(smem + L::offCF);  // 1/||k_i|| 2^(gamma2_{i | 15} - gamma2_i)
   // Decay tables of a value head, over the 16-bit Tm (not in use while A and P are built):
   // Es[b][r][c] = 2^(gamma2_{16b+r} - gamma2_{16b+c}) / ||k_{16b+c}|| for c <= r (else 0), and
-  // rfs[t][b] = 2^(gamma2_t - gamma2_{16b+15}) for the blocks b below t's own
+  // rfs[b][t] = 2^(gamma2_t - gamma2_{16b+15}) for the blocks b below t's own
   float* Es = reinterpret_cast<float*>(smem + L::offTb);  // [4][16][LDE]
-  float* rfs = Es + 4 * 16 * LDE;                          // [64][4]
+  float* rfs = Es + 4 * 16 * LDE;                          // [4][64]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kKBlocks = DK > 64 ? 2 : 1;
@@ -381,7 +384,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         for (int bl = 0; bl < 4; ++bl)  // Es[bl][r][c]
           Es[(16 * bl + r) * LDE + c] = c <= r ? exp2f(g2[16 * bl + r] - g2[16 * bl + c]) * rnk[16 * bl + c] : 0.f;
         {
-          const int t = tid >> 2, bl = tid & 3;
+          const int t = tid & 63, bl = tid >> 6;  // rfs[bl][t] = rfs[tid]
           rfs[tid] = bl < (t >> 4) ? exp2f(g2[t] - g2[16 * bl + 15]) : 0.f;
         }
         if (tid < kChunk) cfs[tid] = rnk[tid] * exp2f(g2[tid | 15] - g2[tid]);  // warps 0 and 1: tokens tid
@@ -408,7 +411,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             float v[16];
             tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + cb, v);
             const float* fp = own ? Es + t * LDE : cfs + cb;  // column factors of this row
-            const float s = own ? sc : below ? sc * rfs[4 * t + (cb >> 4)] : 0.f;
+            const float s = own ? sc : below ? sc * rfs[(cb >> 4) * kChunk + t] : 0.f;
 #pragma unroll
             for (int u = 0; u < 16; u += 4) {
               const float4 f = *reinterpret_cast<const float4*>(fp + u);
@@ -428,7 +431,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           }
           if (isA) {
             if (own) {  // the diagonal block in fp32, for the forward substitution
-              float* arow = Ad + (cb >> 4) * 16 * LDD + (t - cb) * LDD;
+              float* arow = Ad + (cb >> 4) * kDiagStride + (t - cb) * LDD;
 #pragma unroll
               for (int p = 0; p < 4; ++p)
                 *reinterpret_cast<float4*>(arow + 4 * p) = make_float4(o[4 * p], o[4 * p + 1], o[4 * p + 2], o[4 * p + 3]);
@@ -465,7 +468,7 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       // the dependent chain is one FMA per row).
       if (tid < 64) {
         const int blk = tid >> 4, j = tid & 15;
-        const float* Ab = Ad + blk * 16 * LDD;
+        const float* Ab = Ad + blk * kDiagStride;
         float x[16], accv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) { x[i] = (i == j) ? 1.f : 0.f; accv[i] = 0.f; }
