@@ -29,7 +29,6 @@ constexpr int kSegThreads = 256;
 constexpr int kSetupSplit = 8;    // CTAs per (segment, head) in the set-up
 constexpr int kCombineRows = 4;   // state rows per combine CTA
 constexpr int kCombineThreads = 128;
-constexpr int kPhiTile = 32;      // rows of Phi per shared-memory tile
 }  // namespace
 
 // Segment boundaries, their chunk slots, and the two start-state sets of pass A.
@@ -75,15 +74,16 @@ gdn_seg_setup_kernel(const float* __restrict__ init, float* __restrict__ a_init,
 
 // c_init[(b P + p, h)] = S_start(p): the initial state for p = 0, N_0 for p = 1, then
 // S_start(p + 1) = S_start(p) Phi_p + N_p in fp32.  One CTA per (b, h, 4-row slice);
-// thread j forms column j of the 4 rows.  Phi_p streams through shared memory in
-// 32-row tiles (cp.async, double-buffered), so every thread reads it once.
-// grid: (B * Hv, DV / 4).
+// thread j forms column j of the 4 rows.  The transitions Phi_p do not depend on the
+// recurrence, so each goes into shared memory whole (cp.async, two buffers of DK x DK) while
+// the one before it is applied: one load latency for the whole combine instead of one per tile.
+// grid: (B * Hv, DV / 4); dynamic shared memory 2 DK DK floats.
 __global__ void __launch_bounds__(kCombineThreads)
 gdn_seg_combine_kernel(const float* __restrict__ init, const float* __restrict__ n_fin,
                        const float* __restrict__ phi, float* __restrict__ c_init, int B, int P, int Hv, int DV,
                        int DK) {
   __shared__ float srow[kCombineRows][128];
-  __shared__ __align__(16) float tile[2][kPhiTile][128];
+  extern __shared__ __align__(16) float phis[];  // [2][DK][DK]
   const int b = blockIdx.x / Hv, h = blockIdx.x - b * Hv;
   const int r0 = blockIdx.y * kCombineRows;
   const int j = threadIdx.x;
@@ -106,40 +106,34 @@ gdn_seg_combine_kernel(const float* __restrict__ init, const float* __restrict__
     srow[r][j] = x;
     if (col) state_out(1)[(size_t)(r0 + r) * DK + j] = x;
   }
-  const int ntiles = DK / kPhiTile;
-  const int per_row = DK / 4;  // 16-byte pieces per Phi row
-  auto load_tile = [&](const float* ph, int t, int buf) {
-    for (int e = threadIdx.x; e < kPhiTile * per_row; e += kCombineThreads) {
-      const int r = e / per_row, c4 = e - r * per_row;
-      cp_async16(&tile[buf][r][4 * c4], ph + (size_t)(t * kPhiTile + r) * DK + 4 * c4, true);
-    }
+  // Phi_p (p = 1 .. P - 2) into buffer p & 1
+  auto load_phi = [&](int p) {
+    const float* ph = phi + (((size_t)b * P + p) * Hv + h) * n_i;
+    float* dst = phis + (size_t)(p & 1) * n_i;
+    for (size_t e = threadIdx.x; e < n_i / 4; e += kCombineThreads) cp_async16(dst + 4 * e, ph + 4 * e, true);
     cp_async_commit();
   };
+  if (P > 2) load_phi(1);
   for (int p = 1; p + 1 < P; ++p) {
-    const float* ph = phi + (((size_t)b * P + p) * Hv + h) * n_i;
+    const bool next = p + 2 < P;
+    if (next) load_phi(p + 1);  // into the other buffer, read last at p - 1 (barrier below)
     const float* nf = state(n_fin, p);
     float acc[kCombineRows];
 #pragma unroll
     for (int u = 0; u < kCombineRows; ++u) acc[u] = col ? nf[(size_t)(r0 + u) * DK + j] : 0.f;
-    load_tile(ph, 0, 0);
-    for (int t = 0; t < ntiles; ++t) {
-      if (t + 1 < ntiles) {
-        load_tile(ph, t + 1, (t + 1) & 1);
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
-      __syncthreads();  // tile t (and, at t = 0, the previous rows in srow) visible
-      if (col) {
+    if (next) cp_async_wait<1>();
+    else cp_async_wait<0>();
+    __syncthreads();  // Phi_p, and the previous rows in srow, visible
+    if (col) {
+      const float* f = phis + (size_t)(p & 1) * n_i + j;
 #pragma unroll 8
-        for (int kk = 0; kk < kPhiTile; ++kk) {
-          const float f = tile[t & 1][kk][j];
+      for (int kk = 0; kk < DK; ++kk) {
+        const float fk = f[(size_t)kk * DK];
 #pragma unroll
-          for (int u = 0; u < kCombineRows; ++u) acc[u] = fmaf(srow[u][t * kPhiTile + kk], f, acc[u]);
-        }
+        for (int u = 0; u < kCombineRows; ++u) acc[u] = fmaf(srow[u][kk], fk, acc[u]);
       }
-      __syncthreads();  // tile t read before it is refilled
     }
+    __syncthreads();  // Phi_p and srow read before they are overwritten
 #pragma unroll
     for (int u = 0; u < kCombineRows; ++u) {
       srow[u][j] = acc[u];
@@ -158,8 +152,11 @@ cudaError_t launch_seg_setup(const float* init, float* a_init, float* i_init, in
 
 cudaError_t launch_seg_combine(const float* init, const float* n_fin, const float* phi, float* c_init, int B,
                                int P, int Hv, int DV, int DK, cudaStream_t st) {
+  const int smem = 2 * DK * DK * (int)sizeof(float);  // 128 KB at dk = 128
+  cudaError_t e = set_smem_limit_once<gdn_seg_combine_kernel>(2 * 128 * 128 * (int)sizeof(float));
+  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(B * Hv), (unsigned)(DV / kCombineRows));
-  gdn_seg_combine_kernel<<<grid, kCombineThreads, 0, st>>>(init, n_fin, phi, c_init, B, P, Hv, DV, DK);
+  gdn_seg_combine_kernel<<<grid, kCombineThreads, smem, st>>>(init, n_fin, phi, c_init, B, P, Hv, DV, DK);
   return cudaGetLastError();
 }
 
