@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kCombineThreads)
 gdn_seg_combine_kernel(const float* __restrict__ init, const float* __restrict__ n_fin,
                        const float* __restrict__ phi, float* __restrict__ c_init, int B, int P, int Hv, int DV,
                        int DK) {
-  __shared__ float srow[kCombineRows][128];
+  __shared__ __align__(16) float srow[kCombineRows][128];
   extern __shared__ __align__(16) float phis[];  // [2][DK][DK]
   const int b = blockIdx.x / Hv, h = blockIdx.x - b * Hv;
   const int r0 = blockIdx.y * kCombineRows;
@@ -113,24 +113,41 @@ gdn_seg_combine_kernel(const float* __restrict__ init, const float* __restrict__
     for (size_t e = threadIdx.x; e < n_i / 4; e += kCombineThreads) cp_async16(dst + 4 * e, ph + 4 * e, true);
     cp_async_commit();
   };
-  if (P > 2) load_phi(1);
+  // N_p's rows of this CTA, a segment ahead (they do not depend on the recurrence either)
+  float nxt[kCombineRows];
+  auto load_n = [&](int p) {
+    const float* nf = state(n_fin, p);
+#pragma unroll
+    for (int u = 0; u < kCombineRows; ++u) nxt[u] = col ? nf[(size_t)(r0 + u) * DK + j] : 0.f;
+  };
+  if (P > 2) {
+    load_phi(1);
+    load_n(1);
+  }
   for (int p = 1; p + 1 < P; ++p) {
     const bool next = p + 2 < P;
     if (next) load_phi(p + 1);  // into the other buffer, read last at p - 1 (barrier below)
-    const float* nf = state(n_fin, p);
     float acc[kCombineRows];
 #pragma unroll
-    for (int u = 0; u < kCombineRows; ++u) acc[u] = col ? nf[(size_t)(r0 + u) * DK + j] : 0.f;
+    for (int u = 0; u < kCombineRows; ++u) acc[u] = nxt[u];
+    if (next) load_n(p + 1);
     if (next) cp_async_wait<1>();
     else cp_async_wait<0>();
     __syncthreads();  // Phi_p, and the previous rows in srow, visible
-    if (col) {
+    if (col) {  // the rows' entries four at a time (16-byte broadcast loads), in order
       const float* f = phis + (size_t)(p & 1) * n_i + j;
-#pragma unroll 8
-      for (int kk = 0; kk < DK; ++kk) {
-        const float fk = f[(size_t)kk * DK];
+#pragma unroll 2
+      for (int kk = 0; kk < DK; kk += 4) {
+        const float f0 = f[(size_t)kk * DK], f1 = f[(size_t)(kk + 1) * DK], f2 = f[(size_t)(kk + 2) * DK],
+                    f3 = f[(size_t)(kk + 3) * DK];
 #pragma unroll
-        for (int u = 0; u < kCombineRows; ++u) acc[u] = fmaf(srow[u][kk], fk, acc[u]);
+        for (int u = 0; u < kCombineRows; ++u) {
+          const float4 sv = *reinterpret_cast<const float4*>(&srow[u][kk]);
+          acc[u] = fmaf(sv.x, f0, acc[u]);
+          acc[u] = fmaf(sv.y, f1, acc[u]);
+          acc[u] = fmaf(sv.z, f2, acc[u]);
+          acc[u] = fmaf(sv.w, f3, acc[u]);
+        }
       }
     }
     __syncthreads();  // Phi_p and srow read before they are overwritten
