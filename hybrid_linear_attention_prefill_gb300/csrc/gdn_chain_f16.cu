@@ -2,28 +2,35 @@
 //
 // It runs the chunk recurrence of the wide-range state carry (gdn_chain_tc.cu), one CTA per
 // (sequence, value head, 16-, 32- or 64-row slice of S), 8 epilogue warps and 1 issue warp,
-// the slice of S in fp32 registers.  Per 64-token chunk, with Tm = (I + A)^-1 and PT = P Tm
-// from the preparation kernel, gamma = cumsum(g), e = exp(gamma), d = exp(gamma_last - gamma):
+// the slice of S in fp32 registers.  With Tm = (I + A)^-1 and PT = P Tm from the preparation
+// kernel, gamma = cumsum(g), e = exp(gamma), d = exp(gamma_last - gamma), the state update
+// dS^T = K^T diag(d) U = K^T diag(d) Tm R associates as W R with
 //
-//   phase 1   [X; Y] = [K; Q] S^T                       (M = 128 stacked tokens, K = dk)
+//   W = K^T diag(d) Tm        (dk x 64, no dependence on the state)
+//
+// so a chunk takes two dependent tensor-core rounds instead of three:
+//
+//   round 1   [X; Y] = [K; Q] S^T                       (M = 128 stacked tokens, K = dk)
 //             R      = diag(beta) V - diag(beta e) X
-//   phase 2   [U; Z] = [Tm; PT] R                       (M = 128, K = 64)
-//             O      = scale (diag(e) Y + Z)            -> bf16 outputs
-//   phase 3   dS^T   = K^T diag(d) U                    (M = dk = 128, K = 64)
+//   round 2   dS^T   = W R                              (M = dk = 128, K = 64)
 //             S      = e_last S + dS
+//   beside    Z      = PT R, O = scale (diag(e) Y + Z)  -> bf16 outputs, during the next chunk
+//   ahead     W of the next chunk = K^T (diag(d) Tm)    (M = 128, N = 64, K = 64), issued after
+//             round 1; rounded to fp16 by the epilogue warps while the next chunk's round 1 runs
 //
 // the chunk form of S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T, o_t = S_t q_t / sqrt(dk)
 // (the "chunked Gated DeltaNet prefill" of the "Open-Jev-27B-v1.1 native text worker" page,
-// "Validation and optimization scope").
+// "Validation and optimization scope").  Z and W sit off the chain: only the R epilogue and
+// the state update are between one chunk's round 1 and the next.
 //
 // Operands.  Every tensor-core operand is one fp16 value (kind::f16, fp32 accumulate): K and Q
-// come from the preparation kernel as an fp16 image of the shared-memory tile, Tm and PT are
-// fp16 there as well, and the state-side operands S, R and diag(d) U are rounded to fp16 from
-// the fp32 values the epilogues hold.  fp16 keeps 11 significant bits where bf16 keeps 8, so a
+// come from the preparation kernel as an fp16 image of the shared-memory tile, diag(d) Tm and PT
+// are fp16 there as well, and W and the state-side operands S and R are rounded to fp16 from the
+// fp32 values the epilogues hold.  fp16 keeps 11 significant bits where bf16 keeps 8, so a
 // single fp16 operand replaces the bf16 hi + lo pair of the wide-range kernel: the MMAs carry
 // N = DVT columns instead of 2 DVT, and the epilogues read and store half as many.  A float64
 // model of the chunked path with these rounding points puts its errors below those of the bf16
-// kernels (final state 4.6e-4 against 1.05e-3 relative, output 5.7e-4 against 2.5e-3 of the
+// kernels (final state 4.3e-4 against 1.05e-3 relative, output 5.0e-4 against 2.5e-3 of the
 // largest, on a no-decay, beta = 0.999 stress case): bf16 Tm was their largest rounding.
 // fp16 stops at 65504.  An operand beyond it becomes infinite, and that reaches the state, so
 // a (sequence, head) whose final fp32 state is not finite sets status bit 16 (also for
@@ -33,14 +40,21 @@
 // status bit 32.  The wide-range kernel takes values of any magnitude.
 //
 // Shared-memory layouts (tile bases 1024-byte aligned):
-//   [K; Q]   K-major, 128 B swizzle: [dk/64 blocks][128 rows][128 B]; rows 0..63 K, 64..127 Q
-//            (the preparation kernel's image, one bulk copy per block).  The same K rows, read
-//            MN-major (dk contiguous), are phase 3's A operand.
-//   [Tm; PT] K-major, 128 B swizzle: [128 rows][128 B].
-//   S, R, U  MN-major, 128 B swizzle: one 128-byte row per K index (d or token), whose first
-//            DVT fp16 values are the slice's columns (N = DVT of the row's 64).
-//   V        the bf16 value slice: 32 B rows unswizzled (16 rows), 64 B rows with the 64 B
-//            swizzle (32), 128 B rows with the 128 B swizzle (64).
+//   [K; Q]    K-major, 128 B swizzle: [dk/64 blocks][128 rows][128 B]; rows 0..63 K, 64..127 Q
+//             (the preparation kernel's image, one bulk copy per block).  The same K rows, read
+//             MN-major (dk contiguous), are the A operand of the W product.
+//   [dTm; PT] K-major, 128 B swizzle: [128 rows][128 B].  Rows 0..63 read MN-major (one 128-byte
+//             row per token) are the B operand of the W product; rows 64..127 are Z's A operand
+//             (the MMA's M = 128 rows start at row 0, and the Z rows 0..63 are not read).
+//   S, R      MN-major, 128 B swizzle: one 128-byte row per K index (d or token), whose first
+//             DVT fp16 values are the slice's columns (N = DVT of the row's 64).
+//   V         the bf16 value slice: 32 B rows unswizzled (16 rows), 64 B rows with the 64 B
+//             swizzle (32), 128 B rows with the 128 B swizzle (64).
+// TMEM columns: round 1's [X; Y] in two buffers (the outputs read Y a chunk later), dS, Z, the
+// fp32 W of this chunk and the next, and this chunk's W in fp16 as dS's A operand (row d in
+// lane d, two tokens a column): tcgen05.st writes it, so the rounding puts no traffic on shared
+// memory while round 1 reads its operands there (stored to shared memory, it cost the
+// headline step ~8 us).
 #include <cuda_fp16.h>
 
 #include "gdn_tc.cuh"
@@ -52,7 +66,6 @@ namespace {
 
 constexpr int kThreads = 288;  // 8 epilogue warps + 1 issue warp
 constexpr int kEpiThreads = 256;
-constexpr int kParts = 1;  // TMEM accumulators per phase (two in phase 1 measured 2 % slower)
 constexpr uint32_t kMaxPolls = 1u << 24;
 constexpr int kStatusNonFinite = 16;
 constexpr int kStatusSmallState = 32;
@@ -60,35 +73,35 @@ constexpr float kSmallState = 1.f / 4096.f;  // 2^-12: two bits above fp16's sma
 
 template <int DVT>
 struct CfgH {
-  static constexpr int kN = DVT;                       // MMA N: one fp16 column per state row
-  static constexpr int kPS = kN < 32 ? 32 : kN;        // TMEM columns between phase 1's partials
-  static constexpr uint32_t kTmemCols = kParts * kPS;  // 32, 32, 64
+  static constexpr int kN = DVT;                 // MMA N: one fp16 column per state row
+  static constexpr int kPS = kN < 32 ? 32 : kN;  // TMEM columns per accumulator
+  static constexpr uint32_t kColD = 2 * kPS;     // dS (after the two [X; Y] buffers)
+  static constexpr uint32_t kColZ = 3 * kPS;     // Z
+  static constexpr uint32_t kColW = 4 * kPS;       // the next chunk's W, fp32 (64 columns)
+  static constexpr uint32_t kColW16 = kColW + 64;  // W as dS's fp16 A operand, two chunks' (2 x 32 columns)
+  static constexpr uint32_t kTmemCols = 4 * kPS + 128 <= 256 ? 256 : 512;
   static constexpr int kCPT = DVT / 2;                 // state columns per epilogue thread
   static constexpr int kGW = kCPT < 16 ? kCPT : 16;    // columns an epilogue step works on
   static constexpr int kNG = kCPT / kGW;               // steps per thread
   // stage layout (bytes)
   static constexpr int kOffKQ = 0;              // 2 x 16384
-  static constexpr int kOffTP = 32768;          // 16384
+  static constexpr int kOffTP = 32768;          // 16384: [diag(d) Tm; PT]
   static constexpr int kOffV = kOffTP + 16384;  // 64 rows x 2 DVT bytes
   static constexpr int kVBytes = 64 * 2 * DVT;
   static constexpr int kOffG = kOffV + kVBytes;  // 64 fp32
   static constexpr int kOffB = kOffG + 256;      // 64 fp32
   static constexpr int kStage = (kOffB + 256 + 1023) / 1024 * 1024;  // 51, 53, 57 KB
   static constexpr int kStages = 3;  // chunk c + 2 loads during chunk c
-  // B operands after the stages: S (128 d rows), R and dU (64 token rows), 128 B a row
+  // after the stages: S (128 d rows) and R (64 token rows) as B operands, 128 B a row
   static constexpr int kOffS = kStages * kStage;
   static constexpr int kOffR = kOffS + 16384;
-  static constexpr int kOffU = kOffR + 8192;
-  // 64 rows: the Y rows of the output warps wait here between phases 1 and 2 ([32 columns][128 threads])
-  static constexpr int kOffY = kOffU + 8192;
-  static constexpr int kYBytes = DVT == 64 ? 32 * 128 * 4 : 0;
-  static constexpr int kOffBar = kOffY + kYBytes;  // 3 MMA mbarriers, 3 load mbarriers, TMEM base, abort flag
-  static constexpr int kSmemBytes = kOffBar + 64 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int kOffBar = kOffR + 8192;  // 5 MMA mbarriers, kStages load mbarriers, TMEM base, flags
+  static constexpr int kSmemBytes = kOffBar + 128 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t kID_KS = tc::idesc_f16(128, kN, 0, 1);  // A K-major, B MN-major
-  static constexpr uint32_t kID_KT = tc::idesc_f16(128, kN, 1, 1);  // A MN-major, B MN-major
+  static constexpr uint32_t kID_W = tc::idesc_f16(128, 64, 1, 1);   // A MN-major, B MN-major
   static_assert(DVT == 16 || DVT == 32 || DVT == 64, "16, 32 or 64 state rows per CTA");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static_assert((3 + kStages) * 8 <= 48, "mbarriers in the barrier block");
+  static_assert((5 + kStages) * 8 + 16 <= 128, "mbarriers and flags in the barrier block");
 };
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -96,46 +109,12 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// W columns (8 or 16) of the warp's 32 TMEM lanes, summed over NP (1 or 2) accumulators PS
-// columns apart.  The loads and their wait are one statement, so no use of the results can be
-// scheduled before the wait.
-template <int NP, int PS, int W>
-__device__ __forceinline__ void tmem_sum(uint32_t taddr, float (&acc)[W]) {
-  static_assert(NP == 1 || NP == 2, "one or two accumulators");
-  if constexpr (W == 8 && NP == 1) {
-    tc::tmem_ld8(taddr, acc);
-  } else if constexpr (W == 16 && NP == 1) {
-    tc::tmem_ld16(taddr, acc);
-  } else if constexpr (W == 8) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr), "r"(taddr + PS)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = __uint_as_float(r[i]) + __uint_as_float(r[8 + i]);
-  } else {
-    static_assert(W == 16, "8 or 16 columns");
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr), "r"(taddr + PS)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(r[i]) + __uint_as_float(r[16 + i]);
-  }
+// W (8 or 16) consecutive fp32 columns of the warp's 32 TMEM lanes.
+template <int W>
+__device__ __forceinline__ void tmem_cols(uint32_t taddr, float (&acc)[W]) {
+  static_assert(W == 8 || W == 16, "8 or 16 columns");
+  if constexpr (W == 8) tc::tmem_ld8(taddr, acc);
+  else tc::tmem_ld16(taddr, acc);
 }
 
 // W fp16 values at columns c0 .. c0 + W - 1 (c0 a multiple of 8) of operand row `row`:
@@ -196,7 +175,7 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     extern __shared__ unsigned char smem_raw[];
     const uint32_t r = smem_u32(smem_raw);
     uint64_t* bb = reinterpret_cast<uint64_t*>(smem_raw + (((r + 1023u) & ~1023u) - r) + C::kOffBar);
-    for (int i = 0; i < 3 + C::kStages; ++i) tc::mbar_init(&bb[i], 1);
+    for (int i = 0; i < 5 + C::kStages; ++i) tc::mbar_init(&bb[i], 1);
     tc::fence_mbar_init();
   }
   // Launched as a programmatic dependent of the kernel before it in the stream (the preparation
@@ -209,11 +188,16 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
   unsigned char* sm = smem_raw + pad;
   const uint32_t sb = raw_s + pad;  // shared-window address of sm
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);  // [0..2] MMA phases
-  uint64_t* full = bars + 3;                                       // [0..kStages) stage loaded
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffBar + 48);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kOffBar + 52);
-  int* state_max = reinterpret_cast<int*>(sm + C::kOffBar + 56);  // bits of the largest |S| (non-negative floats order as ints)
+  // [0] round 1, [1] dS, [2] Z: each completes once per chunk.  [3 + (j & 1)] the W of the
+  // launch's chunk j.  W is issued before the barrier after which the epilogue warps wait for the
+  // previous chunk's W, so one barrier could complete twice before a late warp polls it, and
+  // its parity would then name a phase still to come; with two, the next completion of either
+  // is issued only after every warp has passed the chunk's second barrier.
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* full = bars + 5;  // [0..kStages) stage loaded
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffBar + 8 * (5 + C::kStages));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* state_max = reinterpret_cast<int*>(tmem_slot + 2);  // bits of the largest |S| (non-negative floats order as ints)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 8;
@@ -238,8 +222,7 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
   const int h = h_base + hy;
   const int hk = h / (Hv / Hk);
   const float scale = rsqrtf((float)DK);
-  constexpr int kP1 = DK / 16 < kParts ? DK / 16 : kParts;  // partials used by phase 1
-  constexpr int kKBlocks = DK > 64 ? 2 : 1;                  // 64-wide d blocks per tile
+  constexpr int kKBlocks = DK > 64 ? 2 : 1;  // 64-wide d blocks per tile
   constexpr uint32_t kTxBytes = kKBlocks * 16384 + C::kVBytes + 16384;
   constexpr int kAhead = C::kStages - 1;  // chunks whose tiles are in flight ahead of the current one
   constexpr int kCPT = C::kCPT, kGW = C::kGW, kNG = C::kNG;
@@ -267,7 +250,7 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     tc::prefetch_tensormap(&tm_v);
     tc::prefetch_tensormap(&tm_w);
   }
-  if (kKBlocks == 1 && !issuer) {  // phase 3 reads all 128 rows of K^T: the rows d >= 64 stay zero
+  if (kKBlocks == 1 && !issuer) {  // the W product reads all 128 rows of K^T: the rows d >= 64 stay zero
     for (int e = tid; e < C::kStages * 1024; e += kEpiThreads) {
       const int stg = e >> 10, w = e & 1023;
       *reinterpret_cast<uint4*>(sm + stg * C::kStage + C::kOffKQ + 16384 + w * 16) = make_uint4(0, 0, 0, 0);
@@ -299,8 +282,8 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     tc::mbar_arrive_expect_tx(&full[stg], kTxBytes);
 #pragma unroll
     for (int db = 0; db < kKBlocks; ++db) tc::bulk_load(st + C::kOffKQ + db * 16384, kq + db * 16384, 16384, &full[stg]);
-    tc::tma_load_3d(st + C::kOffV, &tm_v, dv0, h, t0, &full[stg]);
     tc::tma_load_2d(st + C::kOffTP, &tm_w, 0, (int)(((long long)(slot0 + c) * Hv + h) * 128), &full[stg]);
+    tc::tma_load_3d(st + C::kOffV, &tm_v, dv0, h, t0, &full[stg]);
   };
   auto load_scalars = [&](int c, int stg) {
     unsigned char* st = sm + stg * C::kStage;
@@ -312,42 +295,83 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
       cp_async4(st + C::kOffB + 4 * tid, beta + off, ok);
     }
   };
+  // W = K^T (diag(d) Tm) of the chunk in stage stg: A the K rows read MN-major, B the diag(d) Tm
+  // rows read MN-major (one 128-byte row per token), fp32 into TMEM columns kColW .. + 63.
+  auto issue_w = [&](int stg, int wb) {  // wb: the chunk's position in the launch, mod 2
+    const uint32_t base = sb + (uint32_t)(stg * C::kStage);
+    const uint64_t ka = tc::sdesc(base + C::kOffKQ, 16384, 1024, tc::kSw128);
+    const uint64_t tb = tc::sdesc(base + C::kOffTP, 8192, 1024, tc::kSw128);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      tc::mma_bf16(tmem + C::kColW, ka + (uint64_t)((ks * 2048) >> 4), tb + (uint64_t)((ks * 2048) >> 4), C::kID_W,
+                   ks > 0);
+    tc::commit(&bars[3 + wb]);
+  };
+  // The W of the launch's chunk j to fp16 (epilogue warps): rows d = 32 q4 + lane, tokens
+  // 32 half .. + 31, into the chunk's W buffer in TMEM.  The stores are complete when it returns.
+  auto convert_w = [&](int j) {
+    if (!tc::mbar_wait(&bars[3 + (j & 1)], (uint32_t)((j >> 1) & 1), kMaxPolls)) {
+      *abort_flag = 1;
+      atomicOr(err, 1);
+    }
+    tc::fence_after();
+    float w0[16], w1[16];
+    tc::tmem_ld16(tq + C::kColW + 32 * half, w0);
+    tc::tmem_ld16(tq + C::kColW + 32 * half + 16, w1);
+    uint32_t h16[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      h16[i] = pack_h2(w0[2 * i], w0[2 * i + 1]);
+      h16[8 + i] = pack_h2(w1[2 * i], w1[2 * i + 1]);
+    }
+    tc::tmem_st16(tq + C::kColW16 + 32 * (j & 1) + 16 * half, h16);
+  };
 
   if (c1 > c0) {
-    if (issuer && lane == 0)
+    if (issuer && lane == 0) {
       for (int a = 0; a < kAhead && c0 + a < c1; ++a) load_tiles(c0 + a, a);
+      // the first chunk's W (the later ones are formed a chunk ahead)
+      if (!tc::mbar_wait(&full[0], 0u, kMaxPolls)) {
+        *abort_flag = 1;
+        atomicOr(err, 2);
+      } else {
+        issue_w(0, 0);
+      }
+    }
     load_scalars(c0, 0);
   }
   cp_async_commit();
+  // the first chunk's W to fp16 (the later ones are rounded a chunk ahead, while the chunk
+  // before forms its dS), before the issuing thread reuses the fp32 W columns
+  __syncthreads();
+  if (c1 > c0 && !issuer && !*abort_flag) convert_w(0);
+  tc::fence_before();
 
-  const int tok = 32 * (q4 & 1) + lane;  // this thread's token in phases 1-2
+  const int tok = 32 * (q4 & 1) + lane;  // this thread's token in the R and output epilogues
   // shared-memory descriptors of the operands at stage 0 / their buffers (the issuer's MMAs)
-  const uint64_t dKQ0 = tc::sdesc(sb + C::kOffKQ, 16, 1024, tc::kSw128);     // [K; Q], K-major
-  const uint64_t dKT0 = tc::sdesc(sb + C::kOffKQ, 16384, 1024, tc::kSw128);  // K^T, MN-major
-  const uint64_t dTP0 = tc::sdesc(sb + C::kOffTP, 16, 1024, tc::kSw128);     // [Tm; PT], K-major
-  const uint64_t dS = tc::sdesc(sb + C::kOffS, 16384, 1024, tc::kSw128);     // S, MN-major
-  const uint64_t dR = tc::sdesc(sb + C::kOffR, 8192, 1024, tc::kSw128);      // R, MN-major
-  const uint64_t dU = tc::sdesc(sb + C::kOffU, 8192, 1024, tc::kSw128);      // dU, MN-major
+  const uint64_t dKQ0 = tc::sdesc(sb + C::kOffKQ, 16, 1024, tc::kSw128);  // [K; Q], K-major
+  const uint64_t dTP0 = tc::sdesc(sb + C::kOffTP, 16, 1024, tc::kSw128);  // [dTm; PT], K-major
+  const uint64_t dS = tc::sdesc(sb + C::kOffS, 16384, 1024, tc::kSw128);  // S, MN-major
+  const uint64_t dR = tc::sdesc(sb + C::kOffR, 8192, 1024, tc::kSw128);   // R, MN-major
+  // the outputs of the chunk before: its e, token count and output row
+  float e_prev = 0.f;
+  int n_prev = 0;
+  __nv_bfloat16* orow_prev = out;
   bool aborted = false;
   int c = c0;
   for (; c < c1; ++c) {
     const int ci = c - c0;  // position in this launch: stage and barrier phases
     const int stg = ci % C::kStages;
     const uint32_t par = (uint32_t)(ci & 1);
+    const uint32_t col1 = (uint32_t)C::kPS * par;  // this chunk's [X; Y] buffer
     unsigned char* st = sm + stg * C::kStage;
     cp_async_wait<0>();
-    // The stage's tiles: the thread that issued their copies waits for them, then the barrier
-    // below publishes them to every thread (it makes the accesses that thread requested and saw
-    // complete visible to all the CTA's threads).  The epilogue warps read the value slice after
-    // that barrier without waiting themselves: 256 waits on a completed phase cost the chunk step
-    // ~4 % at the headline size.
-    if (issuer && lane == 0 && !tc::mbar_wait(&full[stg], (uint32_t)((ci / C::kStages) & 1), kMaxPolls)) {
-      *abort_flag = 1;
-      atomicOr(err, 2);
-    }
+    // The stage's tiles: the issuing thread waited for them before forming this chunk's W (a
+    // chunk earlier), and the barrier below publishes them to every thread (it makes the
+    // accesses that thread requested and saw complete visible to all the CTA's threads).
     __syncthreads();
     // Every thread reads the abort flag right after each barrier, so all of them leave the loop
-    // at the same barrier; the issuing thread acts on it after issuing that phase's MMAs (which
+    // at the same barrier; the issuing thread acts on it after issuing that round's MMAs (which
     // an abort makes harmless), so the read is off its path to the tensor core.
     const int ab_top = *abort_flag;
 
@@ -355,48 +379,47 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
       // Descriptors: this stage's bases plus each MMA's offset, added to the start-address field
       // (byte offset / 16; shared addresses stay below 2^18, so the 14-bit field does not carry).
       const uint64_t dKQ = dKQ0 + (uint64_t)((uint32_t)(stg * C::kStage) >> 4);
-      const uint64_t dKT = dKT0 + (uint64_t)((uint32_t)(stg * C::kStage) >> 4);
       const uint64_t dTP = dTP0 + (uint64_t)((uint32_t)(stg * C::kStage) >> 4);
-      // ---- phase 1: [X; Y] = [K; Q] S^T --------------------------------------------
+      // ---- round 1: [X; Y] = [K; Q] S^T ---------------------------------------------
       if (lane == 0) {
         tc::fence_after();
 #pragma unroll
         for (int ks = 0; ks < DK / 16; ++ks) {
           const uint64_t a = dKQ + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
           const uint64_t bd = dS + (uint64_t)((ks * 2048) >> 4);
-          tc::mma_bf16(tmem + C::kPS * (ks % kP1), a, bd, C::kID_KS, ks >= kP1);
+          tc::mma_bf16(tmem + col1, a, bd, C::kID_KS, ks > 0);
         }
         tc::commit(&bars[0]);
-        // stage (ci + kAhead) % kStages = (ci - 1) % kStages was last read by the previous
-        // chunk's MMAs, which are done
-        if (c + kAhead < c1) load_tiles(c + kAhead, (ci + kAhead) % C::kStages);
+        if (c + 1 < c1) {
+          const int s1 = (ci + 1) % C::kStages;
+          if (!tc::mbar_wait(&full[s1], (uint32_t)(((ci + 1) / C::kStages) & 1), kMaxPolls)) {
+            *abort_flag = 1;
+            atomicOr(err, 2);
+          } else {
+            issue_w(s1, (ci + 1) & 1);
+          }
+        }
       }
       __syncwarp();
       if (ab_top) { aborted = true; break; }
-      __syncthreads();  // R written
+      __syncthreads();  // R and this chunk's W written
       const int ab_r = *abort_flag;
-      // ---- phase 2: [U; Z] = [Tm; PT] R ---------------------------------------------
+      // ---- round 2: dS^T = W R; then Z = PT R and the next chunk's W ----------------
       if (lane == 0) {
         tc::fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem, dTP + (uint64_t)((ks * 32) >> 4), dR + (uint64_t)((ks * 2048) >> 4), C::kID_KS, ks > 0);
+          tc::mma_f16_ta(tmem + C::kColD, tmem + C::kColW16 + 32 * par + 8 * ks, dR + (uint64_t)((ks * 2048) >> 4),
+                         C::kID_KS, ks > 0);
         tc::commit(&bars[1]);
-      }
-      __syncwarp();
-      if (ab_r) { aborted = true; break; }
-      __syncthreads();  // dU written
-      const int ab_d = *abort_flag;
-      // ---- phase 3: dS^T = K^T dU ---------------------------------------------------
-      if (lane == 0) {
-        tc::fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem, dKT + (uint64_t)((ks * 2048) >> 4), dU + (uint64_t)((ks * 2048) >> 4), C::kID_KT, ks > 0);
+          tc::mma_bf16(tmem + C::kColZ, dTP + (uint64_t)((ks * 32) >> 4), dR + (uint64_t)((ks * 2048) >> 4), C::kID_KS,
+                       ks > 0);
         tc::commit(&bars[2]);
       }
       __syncwarp();
-      if (ab_d) { aborted = true; break; }
+      if (ab_r) { aborted = true; break; }
       continue;
     }
 
@@ -419,111 +442,112 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     const float glast = __shfl_sync(0xffffffffu, g1, 31);
     const float gam = (q4 & 1) ? g1 : g0;
     const float e_t = expf(gam);
-    const float d_t = expf(glast - gam);
     const float eC = expf(glast);
-    const float b_t = bs[tok];
 
-    // ---- phase-1 epilogue: R = beta V - beta e X (rows 0..63), keep Y (rows 64..127)
-    if (!tc::mbar_wait(&bars[0], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
-    tc::fence_after();
-    // Y of the output warps (q4 >= 2) until phase 2: in registers (16, 32 rows), or in shared
-    // memory (64 rows; column-major over the 128 output threads)
-    float y[kNG][kGW];
-    float* ys = reinterpret_cast<float*>(sm + C::kOffY) + (q4 >= 2 ? 32 * (q4 - 2) + lane + 64 * half : 0);
+    if (q4 < 2) {
+      // ---- R = beta V - beta e X (rows 0..63 of round 1) ----------------------------------
+      const float b_t = bs[tok];
+      if (!tc::mbar_wait(&bars[0], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
+      tc::fence_after();
 #pragma unroll
-    for (int gg = 0; gg < kNG; ++gg) {
-      const int cc = kCPT * half + kGW * gg;  // slice column of this step
-      float acc[kGW];
-      tmem_sum<kP1, C::kPS, kGW>(tq + cc, acc);
-      if (q4 < 2) {
+      for (int gg = 0; gg < kNG; ++gg) {
+        const int cc = kCPT * half + kGW * gg;  // slice column of this step
+        float acc[kGW];
+        tmem_cols<kGW>(tq + col1 + cc, acc);
         float vv[kGW];
         load_v<DVT, kGW>(st + C::kOffV, tok, cc, vv);
         const float be = b_t * e_t;
 #pragma unroll
         for (int i = 0; i < kGW; ++i) acc[i] = b_t * vv[i] - be * acc[i];
         store_h<kGW>(sm + C::kOffR, tok, cc, acc);
-      } else if constexpr (DVT == 64) {
-#pragma unroll
-        for (int i = 0; i < kGW; ++i) ys[(kGW * gg + i) * 128] = acc[i];
-      } else {
-#pragma unroll
-        for (int i = 0; i < kGW; ++i) y[gg][i] = acc[i];
       }
-    }
-    if (q4 < 2) tc::fence_proxy_async();  // R is read by the tensor core next
-    tc::fence_before();
-    __syncthreads();  // R written
-    if (*abort_flag) { aborted = true; break; }
-
-    // ---- phase-2 epilogue: dU (rows 0..63); outputs from Z (rows 64..127) ------------
-    if (!tc::mbar_wait(&bars[1], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
-    tc::fence_after();
-    const int n = min(kChunk, sq.len - c * kChunk);
-    __nv_bfloat16* orow = out + ((size_t)(sq.bos + (long long)c * kChunk + tok) * Hv + h) * DV + dv0;
-    uint32_t o2[kNG][kGW / 2];
+    } else {
+      // ---- the previous chunk's outputs from its Y (rows 64..127 of its round 1) and Z ----
+      if (ci > 0) {
+        if (!tc::mbar_wait(&bars[2], par ^ 1u, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
+        tc::fence_after();
+      }
+      // The stage of the previous chunk is free once its Z is done: its tiles for chunk c + 2.
+      if (warp == 2 && lane == 0 && c + kAhead < c1) load_tiles(c + kAhead, (ci + kAhead) % C::kStages);
+      if (ci > 0) {
+        const uint32_t colp = (uint32_t)C::kPS * (par ^ 1u);
+        const float es = scale * e_prev;
 #pragma unroll
-    for (int gg = 0; gg < kNG; ++gg) {
-      const int cc = kCPT * half + kGW * gg;
-      float acc[kGW];
-      tmem_sum<1, C::kPS, kGW>(tq + cc, acc);
-      if (q4 < 2) {
+        for (int gg = 0; gg < kNG; ++gg) {
+          const int cc = kCPT * half + kGW * gg;
+          float y[kGW], z[kGW];
+          tmem_cols<kGW>(tq + colp + cc, y);
+          tmem_cols<kGW>(tq + C::kColZ + cc, z);
+          if (tok < n_prev) {
 #pragma unroll
-        for (int i = 0; i < kGW; ++i) acc[i] *= d_t;
-        store_h<kGW>(sm + C::kOffU, tok, cc, acc);
-      } else {
-        const float es = scale * e_t;
+            for (int j = 0; j < kGW / 8; ++j) {
+              uint32_t o4[4];
 #pragma unroll
-        for (int p = 0; p < kGW / 2; ++p) {
-          float y0, y1;
-          if constexpr (DVT == 64) { y0 = ys[(kGW * gg + 2 * p) * 128]; y1 = ys[(kGW * gg + 2 * p + 1) * 128]; }
-          else { y0 = y[gg][2 * p]; y1 = y[gg][2 * p + 1]; }
-          o2[gg][p] = pack_bf16(es * y0 + scale * acc[2 * p], es * y1 + scale * acc[2 * p + 1]);
-        }
-        if constexpr (DVT == 64) {  // stored now: the packed outputs do not stay live across the barrier
-          if (tok < n) {
-#pragma unroll
-            for (int j = 0; j < kGW / 8; ++j)
-              *reinterpret_cast<uint4*>(orow + cc + 8 * j) =
-                  make_uint4(o2[gg][4 * j], o2[gg][4 * j + 1], o2[gg][4 * j + 2], o2[gg][4 * j + 3]);
+              for (int p = 0; p < 4; ++p)
+                o4[p] = pack_bf16(es * y[8 * j + 2 * p] + scale * z[8 * j + 2 * p],
+                                  es * y[8 * j + 2 * p + 1] + scale * z[8 * j + 2 * p + 1]);
+              *reinterpret_cast<uint4*>(orow_prev + cc + 8 * j) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
           }
         }
       }
     }
-    if (q4 < 2) tc::fence_proxy_async();  // dU is read by the tensor core next
-    tc::fence_before();
-    __syncthreads();  // dU written
+    if (q4 < 2) tc::fence_proxy_async();  // R is read by the tensor core next
+    tc::fence_before();                     // ... and W, from TMEM
+    __syncthreads();  // R and this chunk's W written
     if (*abort_flag) { aborted = true; break; }
 
-    // outputs go out while the phase-3 MMAs run
-    if (DVT != 64 && q4 >= 2 && tok < n) {
-#pragma unroll
-      for (int gg = 0; gg < kNG; ++gg) {
-        const int cc = kCPT * half + kGW * gg;
-#pragma unroll
-        for (int j = 0; j < kGW / 8; ++j)
-          *reinterpret_cast<uint4*>(orow + cc + 8 * j) =
-              make_uint4(o2[gg][4 * j], o2[gg][4 * j + 1], o2[gg][4 * j + 2], o2[gg][4 * j + 3]);
-      }
-    }
+    // the next chunk's W (issued after this chunk's round 1) to fp16 while dS is formed
+    if (c + 1 < c1) convert_w(ci + 1);
 
-    // ---- phase-3 epilogue: S = e_last S + dS ------------------------------------------
-    if (!tc::mbar_wait(&bars[2], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
+    // ---- S = e_last S + dS ------------------------------------------------------------
+    if (!tc::mbar_wait(&bars[1], par, kMaxPolls)) { *abort_flag = 1; atomicOr(err, 1); }
     tc::fence_after();
 #pragma unroll
     for (int gg = 0; gg < kNG; ++gg) {
       const int cc = kCPT * half + kGW * gg;
       float acc[kGW];
-      tmem_sum<1, C::kPS, kGW>(tq + cc, acc);
+      tmem_cols<kGW>(tq + C::kColD + cc, acc);
 #pragma unroll
       for (int i = 0; i < kGW; ++i) s[kGW * gg + i] = fmaf(eC, s[kGW * gg + i], acc[i]);
       store_h<kGW>(sm + C::kOffS, d, cc, s + kGW * gg);
     }
     tc::fence_proxy_async();  // S is read by the tensor core at the next chunk
     tc::fence_before();
+    e_prev = e_t;
+    n_prev = min(kChunk, sq.len - c * kChunk);
+    orow_prev = out + ((size_t)(sq.bos + (long long)c * kChunk + tok) * Hv + h) * DV + dv0;
   }
 
-  // ---- final state, clean-up -------------------------------------------------------
+  // ---- the last chunk's outputs, final state, clean-up ------------------------------------
   cp_async_wait<0>();
+  if (!aborted && !issuer && q4 >= 2 && c1 > c0) {
+    const uint32_t pl = (uint32_t)((c1 - 1 - c0) & 1);
+    if (tc::mbar_wait(&bars[2], pl, kMaxPolls)) {
+      tc::fence_after();
+      const float es = scale * e_prev;
+#pragma unroll
+      for (int gg = 0; gg < kNG; ++gg) {
+        const int cc = kCPT * half + kGW * gg;
+        float y[kGW], z[kGW];
+        tmem_cols<kGW>(tq + (uint32_t)C::kPS * pl + cc, y);
+        tmem_cols<kGW>(tq + C::kColZ + cc, z);
+        if (tok < n_prev) {
+#pragma unroll
+          for (int j = 0; j < kGW / 8; ++j) {
+            uint32_t o4[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+              o4[p] = pack_bf16(es * y[8 * j + 2 * p] + scale * z[8 * j + 2 * p],
+                                es * y[8 * j + 2 * p + 1] + scale * z[8 * j + 2 * p + 1]);
+            *reinterpret_cast<uint4*>(orow_prev + cc + 8 * j) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+          }
+        }
+      }
+    } else {
+      atomicOr(err, 1);
+    }
+  }
   if (!aborted && !issuer && d < DK) {
     bool finite = true;
     float mx = 0.f;
@@ -545,12 +569,12 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     }
   }
   if (aborted && issuer && lane == 0) {
-    // let MMAs and copies still in flight land before the CTA exits (bounded again)
-    const int ci = c - c0;
-    const uint32_t par = (uint32_t)(ci & 1);
-    for (int i = 0; i < 3; ++i) (void)tc::mbar_wait(&bars[i], par, 1u << 16);
+    // let MMAs and copies still in flight land before the CTA exits (bounded again; a phase
+    // that never started just runs out of polls)
+    for (int i = 0; i < 5; ++i)
+      for (uint32_t p = 0; p < 2; ++p) (void)tc::mbar_wait(&bars[i], p, 1u << 14);
     for (int i = 0; i < C::kStages; ++i)
-      (void)tc::mbar_wait(&full[(ci + i) % C::kStages], (uint32_t)(((ci + i) / C::kStages) & 1), 1u << 16);
+      for (uint32_t p = 0; p < 2; ++p) (void)tc::mbar_wait(&full[i], p, 1u << 14);
   }
   tc::fence_before();
   __syncthreads();

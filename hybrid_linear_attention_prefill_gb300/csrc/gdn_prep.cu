@@ -10,9 +10,10 @@
 //   P  = lower_incl( (Q K^T) * Gamma )                   (decayed intra-chunk scores)
 //   PT = P Tm
 //
-// Tm and PT are stored as 64 x 64 tiles in the workspace -- fp16 for the default
-// state carry, bf16 for the wide-range one -- and the state-carry kernel combines
-// them with the state.  For the fp16 state carry the kernel also writes the chunk's
+// Tm and PT are stored as 64 x 64 tiles in the workspace -- bf16 for the wide-range
+// state carry; for the default one fp16, with Tm's rows scaled by d_t = exp(gamma_last -
+// gamma_t), the diag(d) Tm of its W = K^T diag(d) Tm -- and the state-carry kernel
+// combines them with the state.  For the fp16 state carry the kernel also writes the chunk's
 // k and q rows as fp16 (normalised when asked to), since a tensor-core product takes
 // both operands in one format.  The pages only name the operation (the
 // "chunked Gated DeltaNet prefill" of the "Open-Jev-27B-v1.1 native text
@@ -532,23 +533,34 @@ gdn_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       __syncthreads();
 
       // ---- 16-bit Tm: to shared (for PT) and to the workspace ------------------
-      // fp16 as it stands; the wide-range path's bf16 from those fp16 values
+      // fp16 as it stands for PT; the workspace tile of the fp16 state carry holds diag(d) Tm,
+      // d_t = exp(gamma_last - gamma_t) (its W = K^T diag(d) Tm), each row rounded once more.
+      // The wide-range path's bf16 Tm from those fp16 values, in both places.
       uint16_t* wsT = ws + ((size_t)slot * Hv + h) * (2 * kWsTileElems);
       uint16_t* wsPT = wsT + kWsTileElems;
       for (int e = tid; e < kChunk * 8; e += kPrepThreads) {
         const int r = e >> 3, p = e & 7;
         uint4 v = *reinterpret_cast<const uint4*>(Th + r * LDB + 8 * p);
-        if constexpr (!F16) {
-          uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        if constexpr (F16) {
+          *reinterpret_cast<uint4*>(Tmb + r * LDB + 8 * p) = v;
+          const float dr = exp2f(g2[kChunk - 1] - g2[r]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
+            w4[q] = pack_f16(dr * f.x, dr * f.y);
+          }
+          *reinterpret_cast<uint4*>(wsT + r * kChunk + 8 * p) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        } else {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
             w4[q] = pack16<false>(f.x, f.y);
           }
           v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          *reinterpret_cast<uint4*>(Tmb + r * LDB + 8 * p) = v;
+          *reinterpret_cast<uint4*>(wsT + r * kChunk + 8 * p) = v;
         }
-        *reinterpret_cast<uint4*>(Tmb + r * LDB + 8 * p) = v;
-        *reinterpret_cast<uint4*>(wsT + r * kChunk + 8 * p) = v;
       }
       if (gi == G - 1) tc::fence_proxy_async();  // the inverse's working set is dead: the next tiles may land over it
       __syncthreads();

@@ -4,8 +4,10 @@ The state carry's tensor-core products take 16-bit operands and accumulate in fp
 state and every other quantity stay wide.  This model runs the same chunk-wise recurrence as the
 kernels (the WY / UT-transform form pinned in ``refs.chunked``) in float64 and rounds exactly
 where the kernels round an operand: Tm and PT = P Tm (P and Tm rounded for that product), the
-state S before [X; Y] = [K; Q] S^T, R before [U; Z] = [Tm; PT] R, and diag(d) U before
-dS^T = K^T diag(d) U.  The errors are measured against the float64 oracle on a stress case (no
+state S before [X; Y] = [K; Q] S^T, and R before it is multiplied.  The wide-range state carry
+then forms [U; Z] = [Tm; PT] R and dS^T = K^T diag(d) U with diag(d) U rounded (three rounds);
+the default one forms dS^T = W R with W = K^T diag(d) Tm, rounding diag(d) Tm and W, and
+Z = PT R (two rounds).  The errors are measured against the float64 oracle on a stress case (no
 decay, beta = 0.999, so nothing is forgotten and rounding accumulates over the whole sequence).
 
 What it pins:
@@ -46,9 +48,10 @@ def _round(x, fmt):
     raise ValueError(fmt)
 
 
-def chunked_rounded(inp, fmt_t, fmt_state, C=64):
+def chunked_rounded(inp, fmt_t, fmt_state, two_round=False, C=64):
     """Outputs and final states of the chunk recurrence with the kernels' operand roundings:
-    fmt_t for P, Tm and PT, fmt_state for S, R and diag(d) U."""
+    fmt_t for P, Tm, PT and diag(d) Tm, fmt_state for S, R and diag(d) U (three rounds) or W
+    (two rounds)."""
     q, k, v = bf16_bits_to_f64(inp.q), bf16_bits_to_f64(inp.k), bf16_bits_to_f64(inp.v)
     g, beta = inp.g.astype(np.float64), inp.beta.astype(np.float64)
     Ttot, Hk, dk = q.shape
@@ -77,10 +80,15 @@ def chunked_rounded(inp, fmt_t, fmt_state, C=64):
                 X, Y = K @ S_op.T, Q @ S_op.T
                 R = bt[:, None] * V - (bt * np.exp(gam))[:, None] * X
                 R_op = _round(R, fmt_state)
-                U, Z = Tm_r @ R_op, PT_r @ R_op
-                dU = np.exp(gam[-1] - gam)[:, None] * U
+                Z = PT_r @ R_op
                 out[c0:c1, h] = scale * (np.exp(gam)[:, None] * Y + Z)
-                S = np.exp(gam[-1]) * S + _round(dU, fmt_state).T @ K
+                d = np.exp(gam[-1] - gam)
+                if two_round:
+                    W = _round(K.T @ _round(d[:, None] * Tm_r, fmt_t), fmt_state)
+                    S = np.exp(gam[-1]) * S + (W @ R_op).T
+                else:
+                    dU = d[:, None] * (Tm_r @ R_op)
+                    S = np.exp(gam[-1]) * S + _round(dU, fmt_state).T @ K
                 if fmt_state != "f64":
                     S = S.astype(np.float32).astype(np.float64)  # the state is carried in fp32
             fin[n, h] = S
@@ -97,29 +105,32 @@ def stress():
     return inp, oracle.prefill_inputs(inp)
 
 
-def _errs(stress, fmt_t, fmt_state):
+def _errs(stress, fmt_t, fmt_state, two_round=False):
     inp, (o_ref, s_ref) = stress
-    o, s = chunked_rounded(inp, fmt_t, fmt_state)
+    o, s = chunked_rounded(inp, fmt_t, fmt_state, two_round)
     eo = float(np.max(np.abs(o - o_ref)) / np.max(np.abs(o_ref)))
     es = float(np.linalg.norm(s - s_ref) / np.linalg.norm(s_ref))
     return eo, es
 
 
 def test_fp16_operands_stay_well_inside_the_tolerances_and_below_bf16_hilo(stress):
-    eo16, es16 = _errs(stress, "fp16", "fp16")
     eo_hl, es_hl = _errs(stress, "bf16", "hilo")
-    assert eo16 <= OUT_TOL / 10 and es16 <= STATE_TOL / 2, (eo16, es16)
-    assert es16 < es_hl and eo16 < eo_hl, (eo16, es16, eo_hl, es_hl)
+    for two_round in (True, False):  # the default kernel, and fp16 in the three-round form
+        eo16, es16 = _errs(stress, "fp16", "fp16", two_round)
+        assert eo16 <= OUT_TOL / 10 and es16 <= STATE_TOL / 2, (two_round, eo16, es16)
+        assert es16 < es_hl and eo16 < eo_hl, (two_round, eo16, es16, eo_hl, es_hl)
     assert es_hl <= STATE_TOL and eo_hl <= OUT_TOL  # the wide-range design meets them too
 
 
 def test_bf16_single_state_operands_would_miss_the_state_tolerance(stress):
-    _, es = _errs(stress, "fp16", "bf16")
-    assert es > STATE_TOL, es
+    for two_round in (True, False):
+        _, es = _errs(stress, "fp16", "bf16", two_round)
+        assert es > STATE_TOL, (two_round, es)
 
 
 def test_model_without_rounding_is_the_oracle(stress):
     """With every rounding switched off the model is the exact chunked form, so the errors above
     come from the roundings alone."""
-    eo, es = _errs(stress, "f64", "f64")
-    assert eo <= 1e-10 and es <= 1e-10, (eo, es)
+    for two_round in (True, False):
+        eo, es = _errs(stress, "f64", "f64", two_round)
+        assert eo <= 1e-10 and es <= 1e-10, (two_round, eo, es)
