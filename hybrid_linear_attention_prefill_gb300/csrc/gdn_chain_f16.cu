@@ -627,10 +627,11 @@ cudaError_t launch_chain_f16_dvt(const void* v, const CUtensorMap& mw, const voi
 // two-level scan's inner runs, whose transition states may be legitimately tiny.
 // slice: state rows per CTA, 16, 32 or 64, or 0 for the library's choice.  The MMA issue and
 // the hand-offs of a chunk step do not depend on the width and its epilogues scale with it:
-// measured at 64 chunks, a 16-row step takes 0.91x a 32-row one and a 64-row step 1.41x.  So 64
-// rows when dv allows it and 1.41 x its waves of one CTA per SM are fewer than the 32-row grid's
-// waves (many sequences or heads); 16 rows when twice the 32-row grid still fits one wave (few
-// heads: the chain latency decides, and narrower slices shorten it); 32 otherwise.
+// measured at 64 chunks (state carry alone), a 16-row step takes 0.97-1.0x a 32-row one and a
+// 64-row step 1.19x.  So 64 rows when dv allows it and 1.19 x its waves of one CTA per SM are
+// fewer than the 32-row grid's waves (many sequences or heads); 16 rows when twice the 32-row
+// grid still fits one wave (few heads: the chain latency decides, and narrower slices shorten it
+// a little); 32 otherwise.
 template <int DK>
 cudaError_t launch_chain_f16(const void* v, const float* g, const float* beta, const int32_t* cu,
                              const int32_t* chunk_off, const int32_t* order, const void* ws, const void* ws_kq,
@@ -657,7 +658,7 @@ cudaError_t launch_chain_f16(const void* v, const float* g, const float* beta, c
       return e;
     const long long n32 = (long long)B * (DV / 32) * h_count;
     const long long waves32 = (n32 + sms - 1) / sms, waves64 = (n32 / 2 + sms - 1) / sms;
-    if (DV % 64 == 0 && 141 * waves64 < 100 * waves32) slice = 64;
+    if (DV % 64 == 0 && 119 * waves64 < 100 * waves32) slice = 64;
     else if (2 * n32 <= sms) slice = 16;
   }
   switch (slice) {
