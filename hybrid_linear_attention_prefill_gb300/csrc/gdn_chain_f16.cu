@@ -51,10 +51,10 @@
 //   V         the bf16 value slice: 32 B rows unswizzled (16 rows), 64 B rows with the 64 B
 //             swizzle (32), 128 B rows with the 128 B swizzle (64).
 // TMEM columns: round 1's [X; Y] in two buffers (the outputs read Y a chunk later), dS, Z, the
-// fp32 W of this chunk and the next, and this chunk's W in fp16 as dS's A operand (row d in
-// lane d, two tokens a column): tcgen05.st writes it, so the rounding puts no traffic on shared
-// memory while round 1 reads its operands there (stored to shared memory, it cost the
-// headline step ~8 us).
+// fp32 W of the next chunk, and W in fp16 as dS's A operand (row d in lane d, two tokens a
+// column) for this chunk and the next.  The epilogue warps round the next chunk's W while this
+// chunk's dS is formed and write it with tcgen05.st: rounded into shared memory during round 1
+// instead, it competed with round 1's operand reads and cost the headline step ~8 us.
 #include <cuda_fp16.h>
 
 #include "gdn_tc.cuh"
@@ -402,7 +402,7 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
       }
       __syncwarp();
       if (ab_top) { aborted = true; break; }
-      __syncthreads();  // R and this chunk's W written
+      __syncthreads();  // R written
       const int ab_r = *abort_flag;
       // ---- round 2: dS^T = W R; then Z = PT R and the next chunk's W ----------------
       if (lane == 0) {
@@ -493,8 +493,8 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
       }
     }
     if (q4 < 2) tc::fence_proxy_async();  // R is read by the tensor core next
-    tc::fence_before();                     // ... and W, from TMEM
-    __syncthreads();  // R and this chunk's W written
+    tc::fence_before();
+    __syncthreads();  // R written
     if (*abort_flag) { aborted = true; break; }
 
     // the next chunk's W (issued after this chunk's round 1) to fp16 while dS is formed
