@@ -604,7 +604,7 @@ def main():
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--levels", choices=["auto", "one", "two"], default="auto",
