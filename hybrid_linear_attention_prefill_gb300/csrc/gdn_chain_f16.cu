@@ -390,6 +390,7 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
           tc::mma_bf16(tmem + col1, a, bd, C::kID_KS, ks > 0);
         }
         tc::commit(&bars[0]);
+        // the next chunk's W, once its tiles are in (rounded to fp16 while this chunk's dS runs)
         if (c + 1 < c1) {
           const int s1 = (ci + 1) % C::kStages;
           if (!tc::mbar_wait(&full[s1], (uint32_t)(((ci + 1) / C::kStages) & 1), kMaxPolls)) {
@@ -404,7 +405,7 @@ gdn_chain_f16_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
       if (ab_top) { aborted = true; break; }
       __syncthreads();  // R written
       const int ab_r = *abort_flag;
-      // ---- round 2: dS^T = W R; then Z = PT R and the next chunk's W ----------------
+      // ---- round 2: dS^T = W R; then Z = PT R, off the chain -------------------------
       if (lane == 0) {
         tc::fence_after();
 #pragma unroll
